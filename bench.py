@@ -1,0 +1,372 @@
+#!/usr/bin/env python3
+"""Benchmark: one tree-verify MLA attention layer-step on one GB300 (or N replicas).
+
+A step is one full call of the hot path (split-KV attention kernel + LSE combine)
+over the 64k verify workload: 1 sequence, 65,536-token prefix, a random 16-node
+draft tree, 8 heads, 576-dim bf16 latent rows in a 131,072-slot page_size=1 pool
+reached through a random slot permutation. Inputs are seeded and synthetic.
+
+value  = effective KV GB/s = (visible tokens x (1152-B latent row + 4-B slot entry)) / device time
+         per step, over all ranks (whole job).
+e2e    = the same metric through the public call with host buffers: the step's inputs are
+         copied from pinned host memory and the outputs read back inside the timed region.
+L2     = each step reads a different one of several distinct pools (together larger than L2).
+
+--impl reference times the float64 CPU oracle on this machine's host cores instead
+(the only other program that computes this operation here), on a bounded sample of
+rows per step, extrapolated to the full layer-step.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs/layer-step and effective KV GB/s (% of 8 TB/s HBM) at 64k/185k ctx"
+WORKLOAD = ("64k verify: 1 sequence, 65536-token prefix, random 16-node tree, 8 heads, "
+            "576-dim bf16 latent rows, 131072-slot pool with a random slot permutation, one layer")
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_ROTATION = 4
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK, "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(value, world):
+    """Max of a float over all ranks (identity when world == 1)."""
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value, world):
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_record(fingerprint):
+    """dram read+write bytes of the attention kernel from the committed ncu summary, if it is current."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("fingerprint") != fingerprint:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def cpu_baseline(p, rows_per_step, steps, warmup=0):
+    """Time the float64 oracle on ``rows_per_step`` rows per step; returns (seconds per full layer-step, threads)."""
+    import oracle
+    from speculative_decode_mla_gb300 import workloads as W
+    threads = oracle.max_threads()
+    rng = np.random.default_rng(0)
+    times = []
+    for it in range(warmup + steps):
+        rows = np.sort(rng.choice(p.rows, size=rows_per_step, replace=False))
+        t0 = time.perf_counter()
+        oracle.verify_problem(p, W.SOFTMAX_SCALE, rows=rows)
+        dt = time.perf_counter() - t0
+        if it >= warmup:
+            times.append(dt * p.rows / rows_per_step)
+    return float(np.mean(times)), min(threads, rows_per_step)
+
+
+def run_reference(args):
+    from speculative_decode_mla_gb300 import workloads as W
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    p = W.make_problem("64k")
+    kv_bytes = W.kv_bytes_per_layer_step(p.seq_lens, p.T)
+    rows_per_step = 16
+    t_step, cores = cpu_baseline(p, rows_per_step, args.steps, args.warmup)
+    gbs = kv_bytes / t_step / 1e9
+    sample = (f"{rows_per_step} of {p.rows} query rows per step over the full 65552-position visible set, "
+              f"extrapolated x{p.rows // rows_per_step} to the layer-step")
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+            "us_per_layer_step": t_step * 1e6, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": 1, "seq_len": 65536, "tree_nodes": 16, "heads": 8,
+                       "parallelism": "replicas"},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args):
+    import torch
+    import speculative_decode_mla_gb300 as m
+    from speculative_decode_mla_gb300 import _build
+    from speculative_decode_mla_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    _build.build()
+    m.load_library()
+    stream = torch.cuda.current_stream()
+
+    p = W.make_problem("64k")
+    kv_bytes = W.kv_bytes_per_layer_step(p.seq_lens, p.T)
+    alg_bytes = W.algorithmic_bytes(p.seq_lens, p.T, p.H)
+    flops = W.algorithmic_flops(p.seq_lens, p.T, p.H)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    q = t(p.q.view(np.int16)).view(torch.bfloat16)
+    st, sl, tp = t(p.slot_table), t(p.seq_lens), t(p.tree_parent)
+    pools = [t(p.kv.view(np.int16)).view(torch.bfloat16)]
+    for r in range(1, L2_ROTATION):  # distinct pools with the same logical content (slots permuted)
+        perm = np.random.default_rng(r).permutation(p.num_slots)
+        pools.append(pools[0][torch.from_numpy(perm).to(dev)].contiguous())
+    tables = [st] + [None] * (L2_ROTATION - 1)
+    for r in range(1, L2_ROTATION):
+        perm = np.random.default_rng(r).permutation(p.num_slots)
+        tables[r] = t(np.argsort(perm)[p.slot_table].astype(np.int32))
+    flags = m.DEFAULT_FLAGS
+    desc = m.make_desc(p.B, p.T, p.H, p.num_slots, p.stride, p.max_seq_len, flags=flags)
+    ws = torch.empty(m.workspace_size(desc), dtype=torch.uint8, device=dev)
+    out = torch.empty((p.B * p.T, p.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((p.B * p.T, p.H), dtype=torch.float32, device=dev)
+    sptr = stream.cuda_stream
+    props = torch.cuda.get_device_properties(dev)
+    plan = m.plan(desc, props.multi_processor_count)
+
+    def step(i):
+        r = i % L2_ROTATION
+        rc = m.verify_attn_raw(desc, q.data_ptr(), pools[r].data_ptr(), tables[r].data_ptr(), sl.data_ptr(),
+                               tp.data_ptr(), out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), 0, sptr)
+        if rc:
+            raise m.MLAError(rc, "mla_verify_attn")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        step(i)
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        barrier()
+        # keep the GPU busy long enough for a few clock samples when the steps are short
+        t_end = time.time() + 0.6
+        while time.time() < t_end:
+            for i in range(50):
+                step(i)
+            torch.cuda.synchronize()
+    step_s = ev0.elapsed_time(ev1) / 1e3 / args.steps
+    step_s_max = max_over_ranks(step_s, world)
+
+    # combine kernel alone on this step's own partials (to isolate the attention kernel's time)
+    part_o = ws[: plan.num_splits * p.rows * 512 * 4].view(torch.float32).view(plan.num_splits, p.rows, 512)
+    lse_off = ((plan.num_splits * p.rows * 512 * 4 + 255) // 256) * 256
+    part_l = ws[lse_off: lse_off + plan.num_splits * p.rows * 4].view(torch.float32).view(plan.num_splits, p.rows)
+    for _ in range(3):
+        m.combine(part_o, part_l, out=out.view(p.rows, 512), lse=lse.view(-1), stream=stream)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for _ in range(args.steps):
+        m.combine(part_o, part_l, out=out.view(p.rows, 512), lse=lse.view(-1), stream=stream)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    combine_s = c0.elapsed_time(c1) / 1e3 / args.steps
+    attn_s = max(step_s - combine_s, 1e-9)
+
+    # end to end through the public call with host buffers
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h_q, h_kv = pin(p.q.view(np.int16)), pin(p.kv.view(np.int16))
+    h_st, h_sl, h_tp = pin(p.slot_table), pin(p.seq_lens), pin(p.tree_parent)
+    h_out = torch.empty((p.B * p.T, p.H, 512), dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty((p.B * p.T, p.H), dtype=torch.float32).pin_memory()
+    d_q = torch.empty_like(h_q, device=dev)
+    d_kv, d_st = torch.empty_like(h_kv, device=dev), torch.empty_like(h_st, device=dev)
+    d_sl, d_tp = torch.empty_like(h_sl, device=dev), torch.empty_like(h_tp, device=dev)
+    h2d = sum(x.numel() * x.element_size() for x in (h_q, h_kv, h_st, h_sl, h_tp))
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+
+    def e2e_step():
+        for d_, h_ in ((d_q, h_q), (d_kv, h_kv), (d_st, h_st), (d_sl, h_sl), (d_tp, h_tp)):
+            d_.copy_(h_, non_blocking=True)
+        rc = m.verify_attn_raw(desc, d_q.data_ptr(), d_kv.data_ptr(), d_st.data_ptr(), d_sl.data_ptr(),
+                               d_tp.data_ptr(), out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), 0, sptr)
+        if rc:
+            raise m.MLAError(rc, "mla_verify_attn")
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3 / e2e_steps, world)
+
+    total_kv = sum_over_ranks(kv_bytes, world)
+    value = total_kv / step_s_max / 1e9
+    pk, pk_kind = peaks()
+    peak_hbm = float(pk["hbm_gbs"])
+    achieved = alg_bytes / attn_s / 1e9
+    fp = open(_build.LIB + ".fingerprint").read() if os.path.exists(_build.LIB + ".fingerprint") else None
+    traffic = traffic_record(fp)
+    launches = 2 * args.steps  # attention kernel + combine kernel per step
+
+    base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t_cpu, cores = cpu_baseline(p, rows_per_step=min(p.rows, 32), steps=1)
+        base = {"value": kv_bytes / t_cpu / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                "sample": f"32 of {p.rows} query rows over the full visible set, extrapolated x{p.rows // 32}",
+                "us_per_layer_step": t_cpu * 1e6}
+    clocks = clk.summary()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_s_max * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": 1, "seq_len": 65536, "tree_nodes": 16, "heads": 8,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": f"inputs larger than L2: each step reads the next of {L2_ROTATION} distinct pools",
+                       "kernel": "simt" if plan.kernel == 1 else "tcgen05", "splits": plan.num_splits,
+                       "chunk_tokens": plan.chunk_tokens},
+            "us_per_layer_step": step_s_max * 1e6,
+            "hbm_frac_of_8tbs": value / world / NOMINAL_HBM_GBS,
+            "hbm_frac_of_measured": value / world / peak_hbm,
+            "tensor_frac_of_measured": flops / step_s_max / 1e12 / float(pk["bf16_tflops"]),
+            "attn_kernel_us": attn_s * 1e6, "combine_kernel_us": combine_s * 1e6,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_hbm, "unit": "GB/s",
+                         "frac": achieved / peak_hbm, "traffic": traffic,
+                         "peak_kind": f"{pk_kind} copy bandwidth (burst)",
+                         "algorithmic_bytes_per_launch": alg_bytes},
+            "e2e": {"value": total_kv / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "us_per_step": e2e_s * 1e6},
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        if base is not None:
+            line["cpu_baseline"] = base
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

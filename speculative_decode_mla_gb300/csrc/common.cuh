@@ -1,0 +1,88 @@
+// Shared definitions of the tree-verify MLA attention library (host + device).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mla_verify.h"
+
+namespace mla {
+
+constexpr int kDLatent = 512;            // value width (latent dims)
+constexpr int kDRope = 64;               // RoPE dims appended to each key row
+constexpr int kDK = kDLatent + kDRope;   // 576 bf16 = 1152 bytes per latent row
+constexpr int kTileTokens = 64;          // KV positions per tile; chunks are multiples of it
+constexpr int kMaxNodes = 64;            // tree nodes per sequence (one u64 ancestor mask)
+
+// Everything a kernel needs, by value (a kernel parameter).
+struct VerifyArgs {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* kv;
+  const int32_t* slot_table;
+  const int32_t* seq_lens;
+  const int32_t* tree_parent;
+  float* part_o;      // [splits][rows][512]
+  float* part_lse;    // [splits][rows]
+  int32_t* dev_status;
+  int64_t num_slots;
+  int64_t rows;       // B*T*H
+  int32_t B, T, H, stride, max_seq_len;
+  int32_t chunk, splits, row_tiles, rows_per_tile;
+  int32_t debug;
+  float scale;        // softmax scale
+  float scale_log2;   // softmax scale * log2(e)
+};
+
+// Host-side launchers (each returns a cudaError_t from the launch).
+cudaError_t launch_verify_simt(const VerifyArgs& a, cudaStream_t stream);
+cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream);
+cudaError_t launch_combine(int32_t splits, int64_t rows, int32_t d_v, const float* part_o,
+                           const float* part_lse, void* out, float* lse, int32_t out_dtype,
+                           cudaStream_t stream);
+int tc_kernel_supported();
+
+// Device helpers ------------------------------------------------------------------------------
+__device__ __forceinline__ void report(int32_t* status, int debug, int bit) {
+  if (debug && status) atomicOr(status, bit);
+}
+
+// Prefix length of sequence b, clamped into [0, max_seq_len].
+__device__ __forceinline__ int32_t load_len(const VerifyArgs& a, int b) {
+  int32_t L = a.seq_lens[b];
+  if (L < 0 || L > a.max_seq_len) {
+    report(a.dev_status, a.debug, MLA_CHECK_BAD_LENGTH);
+    L = L < 0 ? 0 : a.max_seq_len;
+  }
+  return L;
+}
+
+// Ancestor-or-self bit set of node i (bit j set iff j == i or j is an ancestor of i).
+// A parent outside [-1, i) is treated as -1 (reported under debug checks).
+__device__ __forceinline__ uint64_t ancestor_mask(const VerifyArgs& a, int b, int i) {
+  const int32_t* par = a.tree_parent + (int64_t)b * a.T;
+  uint64_t m = 0;
+  int j = i;
+  for (int step = 0; step < kMaxNodes && j >= 0; ++step) {
+    m |= 1ull << j;
+    int p = par[j];
+    if (p < -1 || p >= j) {
+      report(a.dev_status, a.debug, MLA_CHECK_BAD_PARENT);
+      p = -1;
+    }
+    j = p;
+  }
+  return m;
+}
+
+// Physical slot of position t of sequence b, clamped into [0, num_slots).
+__device__ __forceinline__ int64_t load_slot(const VerifyArgs& a, int b, int64_t t) {
+  int64_t s = a.slot_table[(int64_t)b * a.stride + t];
+  if (s < 0 || s >= a.num_slots) {
+    report(a.dev_status, a.debug, MLA_CHECK_BAD_SLOT);
+    s = s < 0 ? 0 : a.num_slots - 1;
+  }
+  return s;
+}
+
+}  // namespace mla

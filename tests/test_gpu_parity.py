@@ -1,0 +1,283 @@
+"""GPU parity: the library's kernels against the float64 oracle, through the C ABI.
+
+Bar (written here, per element / per tensor): max-abs error <= 1e-2 and relative L2
+error <= 5e-3 on out (bf16 inputs, fp32 accumulation, bf16 output); |lse| error <= 1e-3.
+Full-size configs are checked on rows sampled across every node, head and sequence.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from _helpers import assert_close, bf16_dev, device_problem, errors, run, to_dev
+from speculative_decode_mla_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+SCALE = W.SOFTMAX_SCALE
+
+
+def kernels():
+    import speculative_decode_mla_gb300 as m
+    return {"simt": m.MLA_FLAG_SIMT}
+
+
+KERNELS = ["simt"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from speculative_decode_mla_gb300 import _build
+    _build.build()
+    oracle.build()
+
+
+def flags_of(name, debug=False):
+    import speculative_decode_mla_gb300 as m
+    return kernels()[name] | (m.MLA_FLAG_DEBUG_CHECKS if debug else 0)
+
+
+def sample_rows(p, per_seq=8, seed=0):
+    rng = np.random.default_rng(seed)
+    R = p.T * p.H
+    rows = []
+    for b in range(p.B):
+        pick = set(rng.choice(R, size=min(per_seq, R), replace=False).tolist())
+        pick |= {0, R - 1}
+        rows += [b * R + r for r in sorted(pick)]
+    return np.array(rows, dtype=np.int64)
+
+
+# ------------------------------------------------------------------ named configs
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_tiny(kernel):
+    p = W.make_problem("tiny")
+    o, l = run(p, flags_of(kernel))
+    ro, rl = oracle.verify_problem(p, SCALE)
+    assert_close(o, l, ro, rl, "tiny")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_64k_all_rows(kernel):
+    p = W.make_problem("64k")
+    o, l = run(p, flags_of(kernel))
+    ro, rl = oracle.verify_problem(p, SCALE)
+    assert_close(o, l, ro, rl, "64k")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_batched_sampled_rows(kernel):
+    p = W.make_problem("batched")
+    o, l = run(p, flags_of(kernel), total_tokens_hint=int((p.seq_lens + p.T).sum()))
+    rows = sample_rows(p, per_seq=6)
+    ro, rl = oracle.verify_problem(p, SCALE, rows=rows)
+    assert_close(o[rows], l[rows], ro, rl, "batched")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("cfg", ["wide", "wide_identity"])
+def test_wide_sampled_rows(kernel, cfg):
+    p = W.make_problem(cfg)
+    o, l = run(p, flags_of(kernel))
+    rows = sample_rows(p, per_seq=48)
+    ro, rl = oracle.verify_problem(p, SCALE, rows=rows)
+    assert_close(o[rows], l[rows], ro, rl, cfg)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_185k_61_layers_sampled(kernel):
+    """61 device-drawn pools (about 13 GB) and one shared slot table; layers 0, 30, 60 checked."""
+    import torch
+    import speculative_decode_mla_gb300 as m
+    cfg = W.CONFIGS["185k"]
+    p0 = W.make_problem(cfg, layer=0, with_kv=False)
+    st, sl, tp = to_dev(p0.slot_table), to_dev(p0.seq_lens), to_dev(p0.tree_parent)
+    pool = torch.empty((cfg.layers, p0.num_slots, W.D_K), dtype=torch.bfloat16, device="cuda")
+    qs = torch.empty((cfg.layers, p0.B * p0.T, p0.H, W.D_K), dtype=torch.bfloat16, device="cuda")
+    for layer in range(cfg.layers):
+        m.fill_normal_bf16(pool[layer], W.tensor_seed(cfg.config_id, layer, W.STREAM_KV))
+        m.fill_normal_bf16(qs[layer], W.tensor_seed(cfg.config_id, layer, W.STREAM_Q))
+    outs = []
+    for layer in range(cfg.layers):
+        o, l = m.verify(qs[layer], pool[layer], st, sl, tp, max_seq_len=p0.max_seq_len, flags=flags_of(kernel))
+        outs.append((o, l))
+    torch.cuda.synchronize()
+    for layer in (0, 30, 60):
+        p = W.make_problem(cfg, layer=layer)
+        o = outs[layer][0].float().cpu().numpy().reshape(p.rows, 512).astype(np.float64)
+        l = outs[layer][1].cpu().numpy().reshape(-1)
+        rows = sample_rows(p, per_seq=10, seed=layer)
+        ro, rl = oracle.verify_problem(p, SCALE, rows=rows)
+        assert_close(o[rows], l[rows], ro, rl, f"185k layer {layer}")
+    del pool, qs
+
+
+# ------------------------------------------------------------------ shapes and edge cases
+SHAPES = [
+    ([0], 1, 1, "random"),          # single visible key
+    ([0], 5, 3, "chain"),           # no prefix, tree only
+    ([1], 1, 16, "random"),
+    ([63], 1, 2, "random"),         # one tile exactly (63 + 1)
+    ([64], 1, 2, "random"),         # tree crosses the tile edge
+    ([130, 7, 1000], 8, 16, "random"),  # ragged batch, 128 rows per sequence
+    ([333], 64, 2, "random"),       # T at its maximum
+    ([77, 300], 3, 5, "star"),      # rows per sequence not a multiple of 8 / 128
+    ([2000], 16, 8, "chain"),       # chain tree: causal tail
+    ([5000, 4500, 6000], 9, 13, "random"),  # several tiles and a ragged tail per sequence
+]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"L{s[0]}-T{s[1]}-H{s[2]}-{s[3]}" for s in SHAPES])
+def test_shapes(kernel, shape):
+    lens, T, H, tree = shape
+    p = W.custom_problem(lens, T, H, tree=tree, seed=len(lens) * 100 + T + H, pool_slack=37, stride_pad=5)
+    o, l = run(p, flags_of(kernel))
+    ro, rl = oracle.verify_problem(p, SCALE)
+    assert_close(o, l, ro, rl, str(shape))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_single_key_returns_value_exactly(kernel):
+    import speculative_decode_mla_gb300 as m
+    p = W.custom_problem([0], 1, 4, seed=3)
+    o, l = run(p, flags_of(kernel), out_dtype=m.MLA_DTYPE_F32)
+    v = W.bf16_bits_to_f32(p.kv[p.slot_table[0, 0]])[:512].astype(np.float64)
+    for h in range(4):
+        assert np.array_equal(o[h], v)
+    ro, rl = oracle.verify_problem(p, SCALE)
+    assert np.abs(l - rl).max() < 1e-4
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("splits", [1, 2, 7, 33])
+def test_split_count_changes_only_rounding(kernel, splits):
+    import speculative_decode_mla_gb300 as m
+    p = W.custom_problem([3000], 16, 8, seed=21)
+    ref_o, ref_l = run(p, flags_of(kernel), out_dtype=m.MLA_DTYPE_F32, num_splits=1)
+    o, l = run(p, flags_of(kernel), out_dtype=m.MLA_DTYPE_F32, num_splits=splits)
+    assert np.abs(o - ref_o).max() <= 2e-5 * max(1.0, np.abs(ref_o).max()) * 10
+    assert np.abs(l - ref_l).max() <= 1e-5
+    ro, rl = oracle.verify_problem(p, SCALE)
+    assert_close(o, l, ro, rl, f"splits={splits}")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_slot_permutation_is_bit_identical(kernel):
+    p = W.custom_problem([2500, 700], 12, 6, seed=22, pool_slack=100)
+    o1, l1 = run(p, flags_of(kernel))
+    rng = np.random.default_rng(1)
+    perm = rng.permutation(p.num_slots)
+    p.kv = p.kv[perm]
+    p.slot_table = np.argsort(perm)[p.slot_table].astype(np.int32)
+    o2, l2 = run(p, flags_of(kernel))
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_constant_value_column_is_one(kernel):
+    import speculative_decode_mla_gb300 as m
+    p = W.custom_problem([4000], 16, 8, seed=23)
+    one = W.f32_to_bf16_bits(np.ones(1, np.float32))[0]
+    p.kv[:, 5] = one
+    p.kv[:, 300] = one
+    o, _ = run(p, flags_of(kernel), out_dtype=m.MLA_DTYPE_F32)
+    assert np.abs(o[:, 5] - 1).max() < 1e-5 and np.abs(o[:, 300] - 1).max() < 1e-5
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_zero_query_gives_mean(kernel):
+    p = W.custom_problem([1500], 8, 4, seed=24)
+    p.q[:] = 0
+    o, l = run(p, flags_of(kernel))
+    ro, rl = oracle.verify_problem(p, SCALE)
+    assert_close(o, l, ro, rl, "q=0")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_f32_output_is_tighter(kernel):
+    import speculative_decode_mla_gb300 as m
+    p = W.custom_problem([6000], 16, 8, seed=25)
+    o, l = run(p, flags_of(kernel), out_dtype=m.MLA_DTYPE_F32)
+    ro, rl = oracle.verify_problem(p, SCALE)
+    err, rel, lerr = errors(o, l, ro, rl)
+    assert rel <= 4e-3 and err <= 5e-3 and lerr <= 1e-3
+
+
+# ------------------------------------------------------------------ device checks and errors
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("fault", ["slot", "parent", "length"])
+def test_debug_checks_report_bad_inputs(kernel, fault):
+    import torch
+    import speculative_decode_mla_gb300 as m
+    p = W.custom_problem([200], 6, 2, seed=26)
+    q, kv, st, sl, tp = device_problem(p)
+    expect = {"slot": m.CHECK_BAD_SLOT, "parent": m.CHECK_BAD_PARENT, "length": m.CHECK_BAD_LENGTH}[fault]
+    if fault == "slot":
+        st[0, 17] = p.num_slots + 5
+    elif fault == "parent":
+        tp[0, 3] = 4
+    else:
+        sl[0] = 250  # above max_seq_len
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(m.MLAError) as ei:
+        m.verify(q, kv, st, sl, tp, max_seq_len=200, flags=flags_of(kernel, debug=True), dev_status=status)
+    assert ei.value.status == -5
+    assert int(status.item()) & expect
+    # without debug checks the bad value is clamped: the call succeeds and nothing faults
+    out, _ = m.verify(q, kv, st, sl, tp, max_seq_len=200, flags=flags_of(kernel))
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_debug_checks_clean_inputs_pass(kernel):
+    import torch
+    import speculative_decode_mla_gb300 as m
+    p = W.custom_problem([500], 8, 4, seed=27)
+    status = torch.full((1,), 123, dtype=torch.int32, device="cuda")
+    dev = device_problem(p)
+    m.verify(*dev, max_seq_len=p.max_seq_len, flags=flags_of(kernel, debug=True), dev_status=status)
+    assert int(status.item()) == 0
+
+
+def test_workspace_too_small_is_rejected():
+    import torch
+    import speculative_decode_mla_gb300 as m
+    p = W.custom_problem([500], 8, 4, seed=28)
+    dev = device_problem(p)
+    ws = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(m.MLAError) as ei:
+        m.verify(*dev, max_seq_len=p.max_seq_len, workspace=ws)
+    assert ei.value.status == -3
+
+
+# ------------------------------------------------------------------ combine entry point
+def test_combine_entry_point_matches_oracle_combine():
+    """Partials of disjoint position windows (as a cross-GPU split would make) merged on the GPU."""
+    import torch
+    import speculative_decode_mla_gb300 as m
+    p = W.custom_problem([900, 40], 8, 4, seed=29)
+    cuts = [0, 100, 101, 500, 940, 10 ** 9]
+    parts = [oracle.verify_problem(p, SCALE, pos_begin=a, pos_end=b) for a, b in zip(cuts[:-1], cuts[1:])]
+    po = np.stack([x[0] for x in parts])
+    pl = np.stack([x[1] for x in parts])
+    ro, rl = oracle.combine(po, pl)
+    o, l = m.combine(torch.from_numpy(po.astype(np.float32)).cuda(), torch.from_numpy(pl.astype(np.float32)).cuda(),
+                     out_dtype=m.MLA_DTYPE_F32)
+    torch.cuda.synchronize()
+    assert np.abs(o.cpu().numpy() - ro).max() < 1e-5
+    finite = np.isfinite(rl)
+    assert np.abs(l.cpu().numpy()[finite] - rl[finite]).max() < 1e-5
+    full_o, full_l = oracle.verify_problem(p, SCALE)
+    assert_close(o.cpu().numpy().astype(np.float64), l.cpu().numpy(), full_o, full_l, "combine")
+
+
+# ------------------------------------------------------------------ input generator
+def test_device_generator_matches_host_bitwise():
+    import torch
+    import speculative_decode_mla_gb300 as m
+    for seed, n, start in [(1, 1000, 0), (W.tensor_seed(2, 60, 1), 4099, 12345), (2 ** 63 + 5, 77, 3)]:
+        t = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+        m.fill_normal_bf16(t, seed, start)
+        got = t.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, W.normal_bf16(seed, n, start=start))

@@ -169,6 +169,41 @@ int mla_verify_combine(int32_t num_splits, int64_t rows, int32_t d_v, const floa
                        const float *part_lse, void *out, float *lse, int32_t out_dtype,
                        mla_stream_t stream);
 
+/*
+ * mla_verify_attn_noalloc -- mla_verify_attn for callers that cannot allocate
+ * device memory. The pages have no counterpart: this is a library convenience.
+ *
+ * Some callers cannot provide the workspace mla_verify_attn asks for: a plugin
+ * whose host framework hands it only the input and output device pointers and
+ * no allocator; a serving process that has already reserved nearly all device
+ * memory for its KV pool, so a cudaMalloc would fail; a latency-critical decode
+ * loop that cannot afford cudaMalloc/cudaFree, which may synchronise the device.
+ * This entry point takes the same arguments as mla_verify_attn minus the
+ * workspace, and uses instead a scratch array of MLA_VERIFY_NOALLOC_SCRATCH_BYTES
+ * that the library itself holds in device memory (a file-scope __device__
+ * array: every GPU on which the library's module is loaded keeps those bytes
+ * until the process exits). It calls no allocation routine of any kind.
+ *
+ * - Set-up: the first call on each device (with that device current) looks up
+ *   the array's device address once and caches it. Make that first call before
+ *   any stream capture begins on that device.
+ * - Limit: when the plan for `desc` on the current device needs more than
+ *   MLA_VERIFY_NOALLOC_SCRATCH_BYTES of workspace (see
+ *   mla_verify_workspace_size), the call returns MLA_ERR_WORKSPACE_TOO_SMALL and
+ *   launches nothing.
+ * - Sharing: every call on a device uses the same array, and the array keeps
+ *   the previous call's contents. Nothing in it needs to start at zero (each
+ *   call writes every partial it reads), but two calls whose kernels overlap in
+ *   time on the GPU (different streams without ordering between them) race on
+ *   the array and corrupt each other's results. Order such calls on one stream
+ *   or with events.
+ * Other arguments, return codes and behaviour are those of mla_verify_attn.
+ */
+#define MLA_VERIFY_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20) /* 32 MiB */
+int mla_verify_attn_noalloc(const mla_verify_desc *desc, const void *q, const void *kv_pool,
+                            const int32_t *slot_table, const int32_t *seq_lens, const int32_t *tree_parent,
+                            void *out, float *lse, int32_t *dev_status, mla_stream_t stream);
+
 /* A static, human-readable description of a status code. */
 const char *mla_verify_status_string(int status);
 

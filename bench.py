@@ -218,11 +218,10 @@ def run_gpu(args):
     ws = torch.empty(m.workspace_size(desc), dtype=torch.uint8, device=dev)
     out = torch.empty((p.B * p.T, p.H, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((p.B * p.T, p.H), dtype=torch.float32, device=dev)
-    sptr = stream.cuda_stream
     props = torch.cuda.get_device_properties(dev)
     plan = m.plan(desc, props.multi_processor_count)
 
-    def step(i):
+    def step(i, sptr):
         r = i % L2_ROTATION
         rc = m.verify_attn_raw(desc, q.data_ptr(), pools[r].data_ptr(), tables[r].data_ptr(), sl.data_ptr(),
                                tp.data_ptr(), out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), 0, sptr)
@@ -235,22 +234,32 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize()
 
+    def capture(fn, n):
+        """A CUDA graph of n calls of fn(i, stream): replays the real calls without host launch overhead."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            sp = torch.cuda.current_stream().cuda_stream
+            for i in range(n):
+                fn(i, sp)
+        return g
+
     for i in range(args.warmup):
-        step(i)
+        step(i, stream.cuda_stream)
+    barrier()
+    graph = capture(step, args.steps)
+    graph.replay()  # untimed: uploads the graph
     barrier()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         time.sleep(0.3)
         ev0.record(stream)
-        for i in range(args.steps):
-            step(i)
+        graph.replay()
         ev1.record(stream)
         barrier()
         # keep the GPU busy long enough for a few clock samples when the steps are short
         t_end = time.time() + 0.6
         while time.time() < t_end:
-            for i in range(50):
-                step(i)
+            graph.replay()
             torch.cuda.synchronize()
     step_s = ev0.elapsed_time(ev1) / 1e3 / args.steps
     step_s_max = max_over_ranks(step_s, world)
@@ -259,12 +268,22 @@ def run_gpu(args):
     part_o = ws[: plan.num_splits * p.rows * 512 * 4].view(torch.float32).view(plan.num_splits, p.rows, 512)
     lse_off = ((plan.num_splits * p.rows * 512 * 4 + 255) // 256) * 256
     part_l = ws[lse_off: lse_off + plan.num_splits * p.rows * 4].view(torch.float32).view(plan.num_splits, p.rows)
-    for _ in range(3):
-        m.combine(part_o, part_l, out=out.view(p.rows, 512), lse=lse.view(-1), stream=stream)
+    o2, l2 = out.view(p.rows, 512).clone(), lse.view(-1).clone()
+
+    def comb(i, sp):
+        rc = m.load_library().mla_verify_combine(plan.num_splits, p.rows, 512, part_o.data_ptr(), part_l.data_ptr(),
+                                                 o2.data_ptr(), l2.data_ptr(), m.MLA_DTYPE_BF16, sp)
+        if rc:
+            raise m.MLAError(rc, "mla_verify_combine")
+
+    for i in range(3):
+        comb(i, stream.cuda_stream)
+    cgraph = capture(comb, args.steps)
+    cgraph.replay()
+    torch.cuda.synchronize()
     c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     c0.record(stream)
-    for _ in range(args.steps):
-        m.combine(part_o, part_l, out=out.view(p.rows, 512), lse=lse.view(-1), stream=stream)
+    cgraph.replay()
     c1.record(stream)
     torch.cuda.synchronize()
     combine_s = c0.elapsed_time(c1) / 1e3 / args.steps
@@ -286,7 +305,8 @@ def run_gpu(args):
         for d_, h_ in ((d_q, h_q), (d_kv, h_kv), (d_st, h_st), (d_sl, h_sl), (d_tp, h_tp)):
             d_.copy_(h_, non_blocking=True)
         rc = m.verify_attn_raw(desc, d_q.data_ptr(), d_kv.data_ptr(), d_st.data_ptr(), d_sl.data_ptr(),
-                               d_tp.data_ptr(), out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), 0, sptr)
+                               d_tp.data_ptr(), out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), 0,
+                               stream.cuda_stream)
         if rc:
             raise m.MLAError(rc, "mla_verify_attn")
         h_out.copy_(out, non_blocking=True)

@@ -90,7 +90,7 @@ typedef struct mla_verify_desc {
   int32_t slot_table_stride;  /* int32 entries per sequence row of slot_table; >= max_seq_len + T */
   int64_t num_slots;          /* rows in kv_pool, 1 .. 2^31 - 1 */
   int32_t max_seq_len;        /* host-known upper bound of every seq_lens[b] */
-  float softmax_scale;        /* finite; 1/sqrt(192) for the absorbed MLA head */
+  float softmax_scale;        /* finite and > 0; 1/sqrt(192) for the absorbed MLA head */
   int32_t out_dtype;          /* MLA_DTYPE_BF16 (default) or MLA_DTYPE_F32 */
   int32_t flags;              /* MLA_FLAG_* */
   int32_t num_splits;         /* 0: planner decides; > 0: force this many KV splits */

@@ -25,8 +25,8 @@ CHECK_BAD_SLOT, CHECK_BAD_PARENT, CHECK_BAD_LENGTH, CHECK_TIMEOUT = 1, 2, 4, 8
 D_LATENT, D_ROPE = 512, 64
 DEFAULT_SCALE = 1.0 / math.sqrt(192.0)
 
-# The kernel a default call runs: flags added to every call unless overridden.
-DEFAULT_FLAGS = MLA_FLAG_SIMT
+# The kernel a default call runs (the tcgen05 kernel): flags used unless a call overrides them.
+DEFAULT_FLAGS = 0
 
 
 class Desc(ctypes.Structure):

@@ -24,7 +24,7 @@ int check_desc(const mla_verify_desc* d) {
   if (d->num_seqs < 1 || d->num_heads < 1 || d->max_seq_len < 0) return MLA_ERR_INVALID_ARGUMENT;
   if (d->num_slots < 1 || d->num_slots > kMaxSlots) return MLA_ERR_INVALID_ARGUMENT;
   if ((int64_t)d->slot_table_stride < (int64_t)d->max_seq_len + d->num_nodes) return MLA_ERR_INVALID_ARGUMENT;
-  if (!isfinite(d->softmax_scale)) return MLA_ERR_INVALID_ARGUMENT;
+  if (!isfinite(d->softmax_scale) || !(d->softmax_scale > 0.f)) return MLA_ERR_INVALID_ARGUMENT;
   if (d->out_dtype != MLA_DTYPE_BF16 && d->out_dtype != MLA_DTYPE_F32) return MLA_ERR_INVALID_ARGUMENT;
   if (d->flags & ~(MLA_FLAG_DEBUG_CHECKS | MLA_FLAG_SIMT)) return MLA_ERR_INVALID_ARGUMENT;
   if (d->num_splits < 0 || d->num_splits > kMaxSplits || d->total_tokens_hint < 0) return MLA_ERR_INVALID_ARGUMENT;

@@ -5,72 +5,98 @@
 //   lse = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * o_s,
 // with parts of lse_s = -inf (nothing visible there) carrying no weight.
 //
-// HBM-bound: per row it reads splits * (4 + 4*d_v) bytes and writes one output
-// row. One CTA of d_v/4 threads per row; each thread owns four consecutive
-// columns (16-byte loads of the partial rows, which sit contiguously per split).
+// Bandwidth-bound on the partials (which normally still sit in L2): per row it
+// reads splits * (4 + 4*d_v) bytes and writes one output row. To keep enough
+// loads in flight, one CTA handles one row and 128 columns; its 8 warps stride
+// over the splits (lane = 4 consecutive columns, 16-byte loads, 4 splits in
+// flight per lane) and are reduced through shared memory at the end.
 #include "common.cuh"
 
 namespace mla {
 namespace {
 
-constexpr int kMaxCombineThreads = 256;  // d_v up to 1024
+constexpr int kCols = 128;   // columns per CTA (32 lanes x 4)
+constexpr int kWarps = 8;
+constexpr int kUnroll = 4;
 
-__global__ void __launch_bounds__(kMaxCombineThreads)
+__global__ void __launch_bounds__(kWarps * 32)
 combine_kernel(int32_t splits, int64_t rows, int32_t d_v, const float* __restrict__ part_o,
                const float* __restrict__ part_lse, void* __restrict__ out, float* __restrict__ lse,
                int32_t out_dtype) {
   const int64_t r = blockIdx.x;
-  if (r >= rows) return;
-  __shared__ float s_w[32];
-  __shared__ float s_red[32];
-  // pass 1: max and sum of exp over the splits (a warp-strided loop, then a block reduction)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float s_red[kWarps];
+  __shared__ float4 s_acc[kWarps][32];
+
+  // 1. max over the splits, then the sum of exp: total = ln sum_s exp(lse_s)
   float m = -INFINITY;
   for (int s = threadIdx.x; s < splits; s += blockDim.x) m = fmaxf(m, part_lse[(int64_t)s * rows + r]);
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m;
+  if (lane == 0) s_red[warp] = m;
   __syncthreads();
-  const int nwarps = (blockDim.x + 31) >> 5;
-  m = -INFINITY;
-  for (int w = 0; w < nwarps; ++w) m = fmaxf(m, s_red[w]);
+  m = s_red[0];
+  for (int w = 1; w < kWarps; ++w) m = fmaxf(m, s_red[w]);
   __syncthreads();
   float z = 0.f;
   if (m != -INFINITY)
     for (int s = threadIdx.x; s < splits; s += blockDim.x) z += expf(part_lse[(int64_t)s * rows + r] - m);
   for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = z;
+  if (lane == 0) s_red[warp] = z;
   __syncthreads();
   z = 0.f;
-  for (int w = 0; w < nwarps; ++w) z += s_w[w];
+  for (int w = 0; w < kWarps; ++w) z += s_red[w];
   const float total = (m == -INFINITY) ? -INFINITY : m + logf(z);
 
-  // pass 2: weighted sum of the partial rows, four columns per thread
-  const int c = threadIdx.x * 4;
+  // 2. weighted sum of this CTA's 128 columns; warp w takes splits w, w + 8, ...
+  const int c = blockIdx.y * kCols + lane * 4;
+  const bool col_ok = c < d_v;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (c < d_v && total != -INFINITY) {
-    for (int s = 0; s < splits; ++s) {
-      const float ls = part_lse[(int64_t)s * rows + r];
-      if (ls == -INFINITY) continue;
-      const float w = expf(ls - total);
-      const float4 v = *reinterpret_cast<const float4*>(part_o + ((int64_t)s * rows + r) * d_v + c);
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
+  if (total != -INFINITY && col_ok) {
+    for (int s0 = warp; s0 < splits; s0 += kWarps * kUnroll) {
+      float w[kUnroll];
+      float4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int s = s0 + u * kWarps;
+        const float ls = s < splits ? part_lse[(int64_t)s * rows + r] : -INFINITY;
+        w[u] = ls == -INFINITY ? 0.f : expf(ls - total);
+        v[u] = ls == -INFINITY ? make_float4(0.f, 0.f, 0.f, 0.f)
+                               : __ldg(reinterpret_cast<const float4*>(part_o + ((int64_t)s * rows + r) * d_v + c));
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        acc.x = fmaf(w[u], v[u].x, acc.x);
+        acc.y = fmaf(w[u], v[u].y, acc.y);
+        acc.z = fmaf(w[u], v[u].z, acc.z);
+        acc.w = fmaf(w[u], v[u].w, acc.w);
+      }
     }
   }
-  if (c < d_v) {
-    if (out_dtype == MLA_DTYPE_F32) {
-      *reinterpret_cast<float4*>(static_cast<float*>(out) + r * d_v + c) = acc;
-    } else {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-      uint2 packed;
-      packed.x = *reinterpret_cast<uint32_t*>(&lo);
-      packed.y = *reinterpret_cast<uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + r * d_v + c) = packed;
+  s_acc[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0) {
+    float4 t = s_acc[0][lane];
+    for (int w = 1; w < kWarps; ++w) {
+      const float4 x = s_acc[w][lane];
+      t.x += x.x;
+      t.y += x.y;
+      t.z += x.z;
+      t.w += x.w;
     }
+    if (col_ok) {
+      if (out_dtype == MLA_DTYPE_F32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(out) + r * d_v + c) = t;
+      } else {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(t.x, t.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(t.z, t.w);
+        uint2 packed;
+        packed.x = *reinterpret_cast<uint32_t*>(&lo);
+        packed.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + r * d_v + c) = packed;
+      }
+    }
+    if (lane == 0 && blockIdx.y == 0 && lse) lse[r] = total;
   }
-  if (threadIdx.x == 0 && lse) lse[r] = total;
 }
 
 }  // namespace
@@ -79,9 +105,8 @@ cudaError_t launch_combine(int32_t splits, int64_t rows, int32_t d_v, const floa
                            const float* part_lse, void* out, float* lse, int32_t out_dtype,
                            cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
-  int threads = ((d_v / 4 + 31) / 32) * 32;
-  combine_kernel<<<dim3((unsigned)rows), threads, 0, stream>>>(splits, rows, d_v, part_o, part_lse, out,
-                                                               lse, out_dtype);
+  dim3 grid((unsigned)rows, (unsigned)((d_v + kCols - 1) / kCols));
+  combine_kernel<<<grid, kWarps * 32, 0, stream>>>(splits, rows, d_v, part_o, part_lse, out, lse, out_dtype);
   return cudaGetLastError();
 }
 

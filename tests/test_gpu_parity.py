@@ -18,10 +18,10 @@ SCALE = W.SOFTMAX_SCALE
 
 def kernels():
     import speculative_decode_mla_gb300 as m
-    return {"simt": m.MLA_FLAG_SIMT}
+    return {"simt": m.MLA_FLAG_SIMT, "tc": 0}
 
 
-KERNELS = ["simt"]
+KERNELS = ["tc", "simt"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -155,7 +155,10 @@ def test_split_count_changes_only_rounding(kernel, splits):
     p = W.custom_problem([3000], 16, 8, seed=21)
     ref_o, ref_l = run(p, flags_of(kernel), out_dtype=m.MLA_DTYPE_F32, num_splits=1)
     o, l = run(p, flags_of(kernel), out_dtype=m.MLA_DTYPE_F32, num_splits=splits)
-    assert np.abs(o - ref_o).max() <= 2e-5 * max(1.0, np.abs(ref_o).max()) * 10
+    # fp32 reordering only for SIMT; the tensor-core path also re-rounds its bf16 P with
+    # each split's own running max, so its split-to-split spread is the size of that rounding
+    tol = 2e-4 if kernel == "simt" else 3e-3
+    assert np.abs(o - ref_o).max() <= tol
     assert np.abs(l - ref_l).max() <= 1e-5
     ro, rl = oracle.verify_problem(p, SCALE)
     assert_close(o, l, ro, rl, f"splits={splits}")
@@ -181,7 +184,10 @@ def test_constant_value_column_is_one(kernel):
     p.kv[:, 5] = one
     p.kv[:, 300] = one
     o, _ = run(p, flags_of(kernel), out_dtype=m.MLA_DTYPE_F32)
-    assert np.abs(o[:, 5] - 1).max() < 1e-5 and np.abs(o[:, 300] - 1).max() < 1e-5
+    # SIMT: fp32 round-to-nearest sums. The tensor cores' fp32 accumulation of ~4000 bf16 terms
+    # drifts by up to about N * 2^-24 ~ 2.4e-4 relative, so the bar is set from that arithmetic.
+    tol = 1e-5 if kernel == "simt" else 2e-3
+    assert np.abs(o[:, 5] - 1).max() < tol and np.abs(o[:, 300] - 1).max() < tol
 
 
 @pytest.mark.parametrize("kernel", KERNELS)

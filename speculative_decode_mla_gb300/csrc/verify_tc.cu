@@ -8,19 +8,25 @@
 //   producer warps 0-3  gather: slot = slot_table[b][t] (page_size=1), then 16-byte
 //                       cp.async of this CTA's 512 value bytes and the 128-byte RoPE
 //                       block of row kv[slot] into a 128B-swizzled (UMMA K-major)
-//                       smem stage; 4 stages.
+//                       smem stage. Warp p owns stage p and tiles p, p+4, ...; it marks
+//                       a tile ready as soon as its own copies have landed.
 //   MMA warp 4          S_r = Q_r K_r^T over the CTA's 288 contraction dims
-//                       (tcgen05.mma kind::f16, A = Q from TMEM, B = K from smem,
-//                       fp32 accumulate in TMEM); then O_r += P V_r (A = P from TMEM,
-//                       B = the same smem stage read MN-major, N = 256).
-//   softmax warps 5-8   one thread per query row: read S_r from TMEM, swap partial
-//                       scores with the partner CTA through distributed shared memory
-//                       (st.async with a byte count on the partner's mbarrier; two
-//                       buffers), S = S_0 + S_1 (the same bits on both CTAs), apply the
+//                       (tcgen05.mma kind::f16, A = Q from TMEM, B = K from smem, fp32
+//                       accumulate in TMEM); O_r += P V_r (A = P from TMEM, B = the same K
+//                       stage read MN-major, N = 256). An event loop issues whichever of S
+//                       and PV is ready, so neither waits on the other.
+//   sender warps 10-13  as soon as S_r is in TMEM, push it to the partner CTA through
+//                       distributed shared memory (st.async with a byte count on the
+//                       partner's mbarrier; two receive buffers per CTA). The partner's
+//                       partial travels in the exp2 domain as fp16 offsets from a per-row
+//                       fp32 reference (the row's largest partial in the tile): half the
+//                       bytes of fp32, most precise for the keys that carry the weight.
+//   softmax warps 6-9   one thread per query row: read S_r from TMEM, add the partner's
+//                       partial (S = S_0 + S_1), apply the
 //                       ancestor bitmask on tree positions, online softmax in the exp2
 //                       domain (O is rescaled only when the running max grows by more
 //                       than 2^8), write P (bf16) to TMEM.
-//   exchange warp 9     tells the partner when this CTA has read a score buffer.
+//   release warp 5      tells the partner when this CTA has read a score buffer.
 //   epilogue            O_r / l goes through 128B-swizzled smem to TMA tensor stores
 //                       (rows past the sequence are clipped by the tensor map); lse to
 //                       the split workspace. The combine kernel merges the splits.
@@ -29,6 +35,7 @@
 // drains what it started, reports MLA_CHECK_TIMEOUT in dev_status when given,
 // writes NaN lse for its rows so the result is visibly invalid, and exits.
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 
@@ -37,26 +44,25 @@ namespace {
 
 constexpr int kRows = 128;              // query rows per tile (MMA M)
 constexpr int kKeys = 64;               // positions per KV tile (S MMA N)
-constexpr int kStages = 4;
-// The producer marks tile t ready kLag tiles after issuing it (once its own copies have landed).
-// kLag must stay below kStages - 1: the slot it waits for is freed by a PV that needs tile t - kStages + 1.
-constexpr int kLag = 2;
+constexpr int kStages = 4;  // one per producer warp
 constexpr int kBlockBytes = kKeys * 128;            // 64 rows x 128 B (one 64-dim block)
 constexpr int kStageBytes = 5 * kBlockBytes;        // 4 value blocks + the RoPE block
-constexpr int kXBytes = kRows * kKeys * 4;          // one partial-score exchange buffer
+constexpr int kXHalfBytes = kRows * kKeys * 2;      // fp16 partial scores of one tile
+constexpr int kXBytes = kXHalfBytes + kRows * 4;    // + one fp32 reference per row
 constexpr int kSmemX = kStages * kStageBytes;       // two exchange buffers follow the stages
 constexpr int kSmemBar = kSmemX + 2 * kXBytes;
 constexpr int kSmemBytes = kSmemBar + 512 + 1024;   // barriers, TMEM slot, tree parents + alignment slack
 constexpr int kEpiBoxBytes = kRows * 128;           // one 32-column fp32 box of O (reuses the stages)
 
-constexpr int kProducerWarps = 4;
+constexpr int kProducerWarps = kStages;
 constexpr int kMmaWarp = 4;
-constexpr int kSoftmaxWarp0 = 5;
-constexpr int kExchangeWarp = 9;
-constexpr int kThreads = 10 * 32;
+constexpr int kReleaseWarp = 5;
+constexpr int kSoftmaxWarp0 = 6;  // warps 6..9: TMEM lane quarters 2, 3, 0, 1
+constexpr int kSenderWarp0 = 10;  // warps 10..13: TMEM lane quarters 2, 3, 0, 1
+constexpr int kThreads = 14 * 32;
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
+constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;  // O 256, S 64, P 32, Q 144 columns
 
 // barrier indices (8 bytes each)
 constexpr int kBarKvFull = 0, kBarKvEmpty = 4, kBarQFull = 8, kBarSFull = 9, kBarSEmpty = 10, kBarPFull = 11,
@@ -67,8 +73,9 @@ constexpr long long kTimeoutCycles = 4000000000ll;  // ~2 s at 2 GHz
 
 // Optional event timeline (built only with -DMLA_TC_TRACE): %globaltimer stamps of pipeline
 // events, kTraceSlots per CTA, into a buffer registered with mla_tc_trace_set.
-constexpr int kTraceSlots = 160;  // 8 fixed events, then 6 per tile for the first 24 tiles, then 4 at the end
-static_assert(kTraceSlots >= 8 + 6 * 24 + 4, "trace slots");
+// 8 fixed events, then 10 per tile for the first 24 tiles (6 softmax, 2 producer, 2 MMA), then 4 at the end
+constexpr int kTraceSlots = 256;
+static_assert(kTraceSlots >= 8 + 10 * 24 + 4, "trace slots");
 #ifdef MLA_TC_TRACE
 }  // namespace
 __device__ unsigned long long* g_mla_trace;
@@ -113,6 +120,16 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
   uint32_t ok;
   asm volatile(
       "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Non-blocking probe of a phase (for the MMA issuer's event loop).
+__device__ __forceinline__ bool mbar_probe(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
       : "memory");
@@ -164,13 +181,13 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// UMMA shared-memory descriptor, 128-byte swizzle (layout type 2), descriptor version 1.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// UMMA shared-memory descriptor, descriptor version 1; layout 2 = 128-byte swizzle, 4 = 64-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout = 2) {
   uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
   d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
   d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
   d |= 1ull << 46;
-  d |= 2ull << 61;
+  d |= (uint64_t)layout << 61;
   return d;
 }
 // Instruction descriptor for kind::f16: bf16 A and B, fp32 D, M x N, B K-major (0) or MN-major (1).
@@ -251,12 +268,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(bar(kBarKvFull + i), kProducerWarps * 32);
+      mbar_init(bar(kBarKvFull + i), 32);  // the owning producer warp
       mbar_init(bar(kBarKvEmpty + i), 1);
     }
     mbar_init(bar(kBarQFull), 4);
     mbar_init(bar(kBarSFull), 1);
-    mbar_init(bar(kBarSEmpty), 4);
+    mbar_init(bar(kBarSEmpty), 8);  // the softmax and the sender warps have both read S
     mbar_init(bar(kBarPFull), 4);
     mbar_init(bar(kBarPEmpty), 1);
     for (int i = 0; i < 2; ++i) {
@@ -294,62 +311,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp < kProducerWarps) {
     // ---------------------------------------------------------------- producer: page_size=1 gather
-    const int key_base = warp * 16;
+    const int stage = warp;
+    const uint32_t sbase = base + stage * kStageBytes;
     const char* kvb = reinterpret_cast<const char*>(a.kv);
-    // slot entries are fetched one tile ahead so their latency hides behind the copies
     const int32_t* tab = a.slot_table + (int64_t)b * a.stride;
-    auto fetch = [&](int t) -> int32_t {
-      const int64_t pos = t0 + (int64_t)t * kKeys + key_base + (lane & 15);
-      return pos < t1 ? tab[pos] : 0;  // positions past the end read row 0 (masked later)
+    // lane l fetches the slots of positions l and l + 32 of a tile; positions past the end
+    // read row 0 (masked later). The next tile's slots are fetched while this one loads.
+    auto fetch = [&](int t, int k) -> int32_t {
+      const int64_t pos = t0 + (int64_t)t * kKeys + k;
+      return (t < ntiles && pos < t1) ? tab[pos] : 0;
     };
-    int32_t slot_next = fetch(0);
-    bool ok = true;
-    for (int t = 0; t < ntiles && ok; ++t) {
-      const int stage = t % kStages;
-      if (t >= kStages && !wait_warp(bar(kBarKvEmpty + stage), ((t / kStages) - 1) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      int32_t slot = slot_next;
-      if (t + 1 < ntiles) slot_next = fetch(t + 1);
-      if (slot < 0 || (int64_t)slot >= a.num_slots) {
+    int32_t next0 = fetch(warp, lane), next1 = fetch(warp, lane + 32);
+    for (int t = warp; t < ntiles; t += kProducerWarps) {
+      if (t >= kStages && !wait_warp(bar(kBarKvEmpty + stage), ((t / kStages) - 1) & 1, abort_flag)) break;
+      int32_t s0 = next0, s1 = next1;
+      next0 = fetch(t + kProducerWarps, lane);
+      next1 = fetch(t + kProducerWarps, lane + 32);
+      if (s0 < 0 || (int64_t)s0 >= a.num_slots || s1 < 0 || (int64_t)s1 >= a.num_slots) {
         report(a.dev_status, a.debug, MLA_CHECK_BAD_SLOT);
-        slot = slot < 0 ? 0 : (int32_t)(a.num_slots - 1);
+        s0 = s0 < 0 ? 0 : (int32_t)min((int64_t)s0, a.num_slots - 1);
+        s1 = s1 < 0 ? 0 : (int32_t)min((int64_t)s1, a.num_slots - 1);
       }
-      const uint32_t sbase = base + stage * kStageBytes;
-#pragma unroll 4
-      for (int k = 0; k < 16; ++k) {  // this CTA's 512 value bytes of one row per instruction
-        const int key = key_base + k;
-        const int64_t sl = __shfl_sync(0xffffffffu, slot, k);
+#pragma unroll 8
+      for (int k = 0; k < kKeys; ++k) {  // this CTA's 512 value bytes of one row per instruction
+        const int64_t sl = __shfl_sync(0xffffffffu, k < 32 ? s0 : s1, k & 31);
         const char* src = kvb + sl * (kDK * 2) + rank * 512 + lane * 16;
         const uint32_t dst =
-            sbase + (lane >> 3) * kBlockBytes + key * 128 + ((((uint32_t)lane & 7u) ^ ((uint32_t)key & 7u)) << 4);
+            sbase + (lane >> 3) * kBlockBytes + k * 128 + ((((uint32_t)lane & 7u) ^ ((uint32_t)k & 7u)) << 4);
         cp_async16(dst, src);
       }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {  // the 128-byte RoPE block of four rows per instruction
-        const int kk = k * 4 + (lane >> 3);
-        const int key = key_base + kk;
-        const int64_t sl = __shfl_sync(0xffffffffu, slot, kk);
+      for (int g = 0; g < kKeys / 4; ++g) {  // the 128-byte RoPE block of four rows per instruction
+        const int k = g * 4 + (lane >> 3);
+        const int64_t sl = __shfl_sync(0xffffffffu, k < 32 ? s0 : s1, k & 31);
         const char* src = kvb + sl * (kDK * 2) + 1024 + (lane & 7) * 16;
         const uint32_t dst =
-            sbase + 4 * kBlockBytes + key * 128 + ((((uint32_t)lane & 7u) ^ ((uint32_t)key & 7u)) << 4);
+            sbase + 4 * kBlockBytes + k * 128 + ((((uint32_t)lane & 7u) ^ ((uint32_t)k & 7u)) << 4);
         cp_async16(dst, src);
       }
       cp_async_commit();
-      if (t == 0 && threadIdx.x == 0) TRACE(2);
-      if (t >= kLag) {
-        cp_async_wait<kLag>();
-        fence_proxy_async();
-        mbar_arrive(bar(kBarKvFull + (t - kLag) % kStages));
-        if (t == kLag && threadIdx.x == 0) TRACE(3);
-      }
+      if (lane == 0 && t < 24) TRACE(14 + 10 * t);  // tile t's copies issued
+      cp_async_wait<0>();
+      fence_proxy_async();
+      mbar_arrive(bar(kBarKvFull + stage));
+      if (lane == 0 && t < 24) TRACE(15 + 10 * t);  // tile t marked ready
     }
     cp_async_wait<0>();
-    fence_proxy_async();
-    if (ok) {
-      for (int t = max(0, ntiles - kLag); t < ntiles; ++t) mbar_arrive(bar(kBarKvFull + t % kStages));
-    }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer (one thread)
     if (lane == 0) {
@@ -358,43 +365,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = wait_bar(bar(kBarQFull), 0, abort_flag);
       TRACE(4);
       tc_fence_after();
-      auto issue_pv = [&](int t) -> bool {
-        if (!wait_bar(bar(kBarPFull), t & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t sbase = base + (t % kStages) * kStageBytes;
+      // Event loop: S(t) needs tile t's stage and S(t-1) read out of TMEM; PV(t) needs S(t)
+      // issued and P(t) written. Whichever is ready goes first, so neither waits on the other.
+      int ns = 0, np = 0;
+      long long idle_since = clock64();
+      while (ok && np < ntiles) {
+        bool progressed = false;
+        if (ns < ntiles && mbar_probe(bar(kBarKvFull + ns % kStages), (ns / kStages) & 1) &&
+            (ns == 0 || mbar_probe(bar(kBarSEmpty), (ns - 1) & 1))) {
+          if (ns == 0) TRACE(5);
+          tc_fence_after();
+          const uint32_t sbase = base + (ns % kStages) * kStageBytes;
+          const uint32_t dS = tmem + kColS;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {  // 16 positions per step; V read MN-major from the same stage
-          const uint64_t bd = smem_desc(sbase + kk * 2048, kBlockBytes, 1024);
-          mma_tmem_a(tmem + kColO, tmem + kColP + kk * 8, bd, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(kBarKvEmpty + t % kStages));
-        mma_commit(bar(kBarPEmpty));
-        return true;
-      };
-      for (int t = 0; t < ntiles && ok; ++t) {
-        const int stage = t % kStages;
-        if (!wait_bar(bar(kBarKvFull + stage), (t / kStages) & 1, abort_flag)) { ok = false; break; }
-        if (t == 0) TRACE(5);
-        if (t > 0 && !wait_bar(bar(kBarSEmpty), (t - 1) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t sbase = base + stage * kStageBytes;
+          for (int j = 0; j < 4; ++j) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = smem_desc(sbase + j * kBlockBytes + kk * 32, 16, 1024);
-            mma_tmem_a(tmem + kColS, tmem + kColQ + j * 32 + kk * 8, bd, idesc_s, (j | kk) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bd = smem_desc(sbase + j * kBlockBytes + kk * 32, 16, 1024);
+              mma_tmem_a(dS, tmem + kColQ + j * 32 + kk * 8, bd, idesc_s, (j | kk) ? 1u : 0u);
+            }
           }
-        }
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {  // this CTA's half of the RoPE dims
-          const uint64_t bd = smem_desc(sbase + 4 * kBlockBytes + (rank * 2 + kk) * 32, 16, 1024);
-          mma_tmem_a(tmem + kColS, tmem + kColQ + 128 + kk * 8, bd, idesc_s, 1u);
+          for (int kk = 0; kk < 2; ++kk) {  // this CTA's half of the RoPE dims
+            const uint64_t bd = smem_desc(sbase + 4 * kBlockBytes + (rank * 2 + kk) * 32, 16, 1024);
+            mma_tmem_a(dS, tmem + kColQ + 128 + kk * 8, bd, idesc_s, 1u);
+          }
+          mma_commit(bar(kBarSFull));
+          if (ns < 24) TRACE(16 + 10 * ns);  // S(ns) issued
+          ++ns;
+          progressed = true;
         }
-        mma_commit(bar(kBarSFull));
-        if (t > 0 && !issue_pv(t - 1)) { ok = false; break; }
+        if (np < ns && mbar_probe(bar(kBarPFull), np & 1)) {
+          tc_fence_after();
+          const uint32_t sbase = base + (np % kStages) * kStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {  // 16 positions per step; V read MN-major from the same stage
+            const uint64_t bd = smem_desc(sbase + kk * 2048, kBlockBytes, 1024);
+            mma_tmem_a(tmem + kColO, tmem + kColP + kk * 8, bd, idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(kBarKvEmpty + np % kStages));
+          mma_commit(bar(kBarPEmpty));
+          if (np < 24) TRACE(17 + 10 * np);  // PV(np) issued
+          ++np;
+          progressed = true;
+        }
+        if (progressed) {
+          idle_since = clock64();
+        } else if (*abort_flag) {
+          ok = false;
+        } else if (clock64() - idle_since > kTimeoutCycles) {
+          *abort_flag = 1;
+          ok = false;
+        }
       }
-      if (ok) ok = issue_pv(ntiles - 1);
       // drain: every MMA issued so far has completed once this barrier flips
       mma_commit(bar(kBarDrain));
       const long long st = clock64();
@@ -402,7 +425,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kExchangeWarp) {
+  } else if (warp == kReleaseWarp) {
     // ---------------------------------------------------------------- score-buffer release to the partner
     if (lane == 0) {
       const uint32_t xempty_remote0 = map_to_cta(bar(kBarXEmpty), peer);
@@ -412,6 +435,71 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+  } else if (warp >= kSenderWarp0) {
+    // ---------------------------------------------------------------- sender warps: S_r to the partner
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
+    const int local_row = row0 + r;
+    uint64_t anc = ~0ull;  // anc*(node): the tree positions this row can see
+    if (local_row < R) {
+      anc = 0;
+      for (int j = local_row / a.H, step = 0; j >= 0 && step < kMaxNodes; j = s_parent[j], ++step) anc |= 1ull << j;
+    }
+    const uint32_t x_remote0 = map_to_cta(base + kSmemX, peer);
+    const uint32_t xfull_remote0 = map_to_cta(bar(kBarXFull), peer);
+    for (int t = 0; t < ntiles; ++t) {
+      const int xb = t & 1;
+      if (!wait_warp(bar(kBarSFull), t & 1, abort_flag)) break;
+      tc_fence_after();
+      uint32_t su[kKeys];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) TMEM_LD16(lane_addr + kColS + c * 16, (su + c * 16));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarSEmpty));
+      // exp2-domain partial, as fp16 offsets from this row's largest partial among the keys
+      // it can see in this tile (so the offsets of the keys that matter are small and exact
+      // enough, and positions past the end never influence the result)
+      float ref = -INFINITY;
+      const int64_t p0 = t0 + (int64_t)t * kKeys;
+      if (p0 + kKeys <= L) {
+#pragma unroll
+        for (int k = 0; k < kKeys; ++k) ref = fmaxf(ref, __uint_as_float(su[k]));
+      } else {
+#pragma unroll
+        for (int k = 0; k < kKeys; ++k) {
+          const int64_t p = p0 + k;
+          if (p < L || (p < N && ((anc >> (p - L)) & 1ull))) ref = fmaxf(ref, __uint_as_float(su[k]));
+        }
+      }
+      ref = (ref == -INFINITY) ? 0.f : ref * a.scale_log2;  // softmax_scale > 0
+      uint32_t hv[kKeys / 2];
+#pragma unroll
+      for (int k = 0; k < kKeys; k += 2) {
+        const __half2 h = __floats2half2_rn(fmaf(__uint_as_float(su[k]), a.scale_log2, -ref),
+                                            fmaf(__uint_as_float(su[k + 1]), a.scale_log2, -ref));
+        hv[k / 2] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      // the partner's buffer xb is free once it has read what this CTA sent two tiles ago
+      if (t >= 2 && !wait_warp(bar(kBarXEmpty + xb), ((t - 2) >> 1) & 1, abort_flag, true)) break;
+      const uint32_t xr = x_remote0 + (uint32_t)(xb * kXBytes);
+      const uint32_t xf = xfull_remote0 + 8u * (uint32_t)xb;
+#pragma unroll
+      for (int j = 0; j < kKeys / 8; ++j) {  // 16-byte chunk j of row r holds keys 8j .. 8j + 7
+        asm volatile(
+            "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                xr + (j * kRows + r) * 16),
+            "r"(hv[4 * j]), "r"(hv[4 * j + 1]), "r"(hv[4 * j + 2]), "r"(hv[4 * j + 3]), "r"(xf)
+            : "memory");
+      }
+      asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                       xr + kXHalfBytes + r * 4),
+                   "r"(__float_as_uint(ref)), "r"(xf)
+                   : "memory");
+      if (warp == kSenderWarp0 && lane == 0 && t < 24) TRACE(10 + 10 * t);
+    }
   } else {
     // ---------------------------------------------------------------- softmax warps, one thread per row
     const int q4 = warp & 3;
@@ -423,21 +511,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int node = valid ? local_row / a.H : 0;
 
     // Q -> TMEM: this CTA's 256 value dims then its 32 RoPE dims, two bf16 per column.
-    // All 36 loads are issued before the first TMEM store so their latencies overlap.
+    // The loads of each half are issued before its TMEM stores so their latencies overlap.
+    const bool q_ok = true;
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(a.q + (valid ? grow : 0) * kDK);
-      uint32_t v[144];
 #pragma unroll
-      for (int chunk = 0; chunk < 36; ++chunk) {  // 16-byte chunks: 0..31 value, 32..35 RoPE
-        const int src = chunk < 32 ? rank * 32 + chunk : 64 + rank * 4 + (chunk - 32);
-        const uint4 x = valid ? __ldg(qrow + src) : make_uint4(0, 0, 0, 0);
-        v[chunk * 4 + 0] = x.x;
-        v[chunk * 4 + 1] = x.y;
-        v[chunk * 4 + 2] = x.z;
-        v[chunk * 4 + 3] = x.w;
+      for (int half = 0; half < 2; ++half) {  // 16-byte chunks [0, 20) then [20, 36): 0..31 value, 32..35 RoPE
+        const int c0 = half * 20, nc = half ? 16 : 20;
+        uint32_t v[80];
+#pragma unroll
+        for (int i = 0; i < nc; ++i) {
+          const int chunk = c0 + i;
+          const int src = chunk < 32 ? rank * 32 + chunk : 64 + rank * 4 + (chunk - 32);
+          const uint4 x = valid ? __ldg(qrow + src) : make_uint4(0, 0, 0, 0);
+          v[i * 4 + 0] = x.x;
+          v[i * 4 + 1] = x.y;
+          v[i * 4 + 2] = x.z;
+          v[i * 4 + 3] = x.w;
+        }
+#pragma unroll
+        for (int c = 0; c < nc / 4; ++c) TMEM_ST16(lane_addr + kColQ + (c0 / 4 + c) * 16, (v + c * 16));
       }
-#pragma unroll
-      for (int c = 0; c < 9; ++c) TMEM_ST16(lane_addr + kColQ + c * 16, (v + c * 16));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -452,16 +546,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int j = node, step = 0; j >= 0 && step < kMaxNodes; j = s_parent[j], ++step) anc |= 1ull << j;
     }
 
-    const uint32_t x_remote0 = map_to_cta(base + kSmemX, peer);
-    const uint32_t xfull_remote0 = map_to_cta(bar(kBarXFull), peer);
     // l_run sums the exact exponentials (for lse); l_bf sums the bf16-rounded P the MMA
     // multiplies with (for normalising O, so a constant value column comes out as exactly 1)
     float m_run = -INFINITY, l_run = 0.f, l_bf = 0.f;
-    bool ok = true;
+    bool ok = q_ok;
     for (int t = 0; t < ntiles && ok; ++t) {
       const int xb = t & 1;
       if (!wait_warp(bar(kBarSFull), t & 1, abort_flag)) { ok = false; break; }
-      if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(8 + 6 * t);
+      if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(8 + 10 * t);
       tc_fence_after();
       float sc[kKeys];
       {
@@ -473,35 +565,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarSEmpty));
-      if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(9 + 6 * t);
+      if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(9 + 10 * t);
 
-      // swap partial scores with the partner: asynchronous remote stores into its buffer xb,
-      // each landing with a byte count on the partner's x_full[xb]
-      if (t >= 2 && !wait_warp(bar(kBarXEmpty + xb), ((t - 2) >> 1) & 1, abort_flag, true)) { ok = false; break; }
-      const uint32_t xr = x_remote0 + (uint32_t)(xb * kXBytes);
-      const uint32_t xf = xfull_remote0 + 8u * (uint32_t)xb;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        asm volatile(
-            "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-                xr + (j * kRows + r) * 16),
-            "f"(sc[4 * j]), "f"(sc[4 * j + 1]), "f"(sc[4 * j + 2]), "f"(sc[4 * j + 3]), "r"(xf)
-            : "memory");
-      }
-      if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(10 + 6 * t);
       if (!wait_warp(bar(kBarXFull + xb), (t >> 1) & 1, abort_flag, true)) { ok = false; break; }
       if (warp == kSoftmaxWarp0 && lane == 0) {
-        if (t < 24) TRACE(11 + 6 * t);
+        if (t < 24) TRACE(11 + 10 * t);
         mbar_arrive_expect_tx(bar(kBarXFull + xb), kXBytes);  // arm this buffer's next use
       }
-      const float4* xbuf = reinterpret_cast<const float4*>(smem + kSmemX + xb * kXBytes);
+      // S (exp2 domain) = own partial * scale_log2 + partner's reference + partner's fp16 offset
+      {
+        const uint8_t* xbuf = smem + kSmemX + xb * kXBytes;
+        const float pref = reinterpret_cast<const float*>(xbuf + kXHalfBytes)[r];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float4 o = xbuf[j * kRows + r];
-        sc[4 * j] += o.x;
-        sc[4 * j + 1] += o.y;
-        sc[4 * j + 2] += o.z;
-        sc[4 * j + 3] += o.w;
+        for (int j = 0; j < kKeys / 8; ++j) {
+          const uint4 w = reinterpret_cast<const uint4*>(xbuf)[j * kRows + r];
+          const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[u]));
+            const int k = 8 * j + 2 * u;
+            sc[k] = fmaf(sc[k], a.scale_log2, f.x + pref);
+            sc[k + 1] = fmaf(sc[k + 1], a.scale_log2, f.y + pref);
+          }
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarXRead + xb));  // the exchange warp releases it to the partner
@@ -519,7 +605,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float mt = sc[0];
 #pragma unroll
       for (int k = 1; k < kKeys; ++k) mt = fmaxf(mt, sc[k]);
-      const float m_new = fmaxf(m_run, mt * a.scale_log2);  // softmax_scale > 0
+      const float m_new = fmaxf(m_run, mt);
       bool rescale = false;
       float alpha = 1.f;
       if (m_new > m_run + 8.f) {  // also the first visible tile (m_run = -inf)
@@ -534,8 +620,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float lsum = 0.f, lbf = 0.f;
 #pragma unroll
       for (int k = 0; k < kKeys; k += 2) {
-        const float e0 = ex2(fmaf(sc[k], a.scale_log2, neg_m));
-        const float e1 = ex2(fmaf(sc[k + 1], a.scale_log2, neg_m));
+        const float e0 = ex2(sc[k] + neg_m);
+        const float e1 = ex2(sc[k + 1] + neg_m);
         const uint32_t pr = pack_bf16(e0, e1);
         lsum += e0 + e1;
         lbf += __uint_as_float(pr << 16) + __uint_as_float(pr & 0xffff0000u);
@@ -545,7 +631,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       l_bf += lbf;
 
       // P -> TMEM once PV of the previous tile has finished with it (and with O)
-      if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(12 + 6 * t);
+      if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(12 + 10 * t);
       if (t > 0) {
         if (!wait_warp(bar(kBarPEmpty), (t - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -570,7 +656,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarPFull));
-      if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(13 + 6 * t);
+      if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(13 + 10 * t);
     }
 
     // epilogue: O_r / l through 128B-swizzled smem boxes (the stage buffers are idle now)

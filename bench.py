@@ -265,14 +265,14 @@ def run_gpu(args):
     step_s_max = max_over_ranks(step_s, world)
 
     # combine kernel alone on this step's own partials (to isolate the attention kernel's time)
-    part_o = ws[: plan.num_splits * p.rows * 512 * 4].view(torch.float32).view(plan.num_splits, p.rows, 512)
-    lse_off = ((plan.num_splits * p.rows * 512 * 4 + 255) // 256) * 256
+    part_o = ws[: plan.num_splits * p.rows * 512 * 2].view(torch.float16).view(plan.num_splits, p.rows, 512)
+    lse_off = ((plan.num_splits * p.rows * 512 * 2 + 255) // 256) * 256
     part_l = ws[lse_off: lse_off + plan.num_splits * p.rows * 4].view(torch.float32).view(plan.num_splits, p.rows)
     o2, l2 = out.view(p.rows, 512).clone(), lse.view(-1).clone()
 
     def comb(i, sp):
-        rc = m.load_library().mla_verify_combine(plan.num_splits, p.rows, 512, part_o.data_ptr(), part_l.data_ptr(),
-                                                 o2.data_ptr(), l2.data_ptr(), m.MLA_DTYPE_BF16, sp)
+        rc = m.load_library().mla_verify_combine(plan.num_splits, p.rows, 512, part_o.data_ptr(), m.MLA_DTYPE_F16,
+                                                 part_l.data_ptr(), o2.data_ptr(), l2.data_ptr(), m.MLA_DTYPE_BF16, sp)
         if rc:
             raise m.MLAError(rc, "mla_verify_combine")
 

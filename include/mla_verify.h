@@ -58,7 +58,8 @@ enum mla_status {
   MLA_ERR_NO_DEVICE = -6          /* no usable sm_103 device is current */
 };
 
-enum mla_dtype { MLA_DTYPE_BF16 = 0, MLA_DTYPE_F32 = 1 };
+/* Element types. out: BF16 or F32. Split partials (mla_verify_combine's part_o): F32 or F16. */
+enum mla_dtype { MLA_DTYPE_BF16 = 0, MLA_DTYPE_F32 = 1, MLA_DTYPE_F16 = 2 };
 
 enum mla_flags {
   /* Check every slot, parent and prefix length on the device, write the findings
@@ -123,8 +124,9 @@ int mla_verify_plan(const mla_verify_desc *desc, int32_t num_sms, mla_verify_pla
  * mla_verify_workspace_size -- device workspace bytes mla_verify_attn needs for
  * `desc` on the current device (queries its SM count). *bytes receives the size.
  * Layout (owned by the library, opaque to the caller): partial outputs
- * float32 [num_splits][B*T*H][512] followed by partial lse float32
- * [num_splits][B*T*H]. Returns MLA_OK, MLA_ERR_INVALID_ARGUMENT, MLA_ERR_UNSUPPORTED
+ * float16 [num_splits][B*T*H][512] (each normalised over its own part, so
+ * |o| <= max |v|), then partial lse float32 [num_splits][B*T*H] at the next
+ * 256-byte boundary. Returns MLA_OK, MLA_ERR_INVALID_ARGUMENT, MLA_ERR_UNSUPPORTED
  * or MLA_ERR_NO_DEVICE.
  */
 int mla_verify_workspace_size(const mla_verify_desc *desc, size_t *bytes);
@@ -158,16 +160,17 @@ int mla_verify_attn(const mla_verify_desc *desc, const void *q, const void *kv_p
  *   lse[r] = ln sum_s exp(part_lse[s][r]);  out[r] = sum_s exp(part_lse[s][r] - lse[r]) * part_o[s][r]
  * Partials with part_lse = -inf carry no weight (and their part_o is not read);
  * a row whose partials are all -inf gets lse = -inf and out = 0.
- *   part_o   device float32 [num_splits][rows][d_v], each normalised over its own part.
+ *   part_o   device [num_splits][rows][d_v], float32 or float16 per part_dtype, each
+ *            normalised over its own part; 16-byte aligned.
  *   part_lse device float32 [num_splits][rows].
  *   out      device [rows][d_v], bf16 or float32 per out_dtype, 16-byte aligned.
  *   lse      device float32 [rows] or NULL.
  * d_v must be a positive multiple of 4. This is also the seam for a split of
  * the KV range across GPUs: each GPU's (o, lse) pair is one partial.
  */
-int mla_verify_combine(int32_t num_splits, int64_t rows, int32_t d_v, const float *part_o,
-                       const float *part_lse, void *out, float *lse, int32_t out_dtype,
-                       mla_stream_t stream);
+int mla_verify_combine(int32_t num_splits, int64_t rows, int32_t d_v, const void *part_o,
+                       int32_t part_dtype, const float *part_lse, void *out, float *lse,
+                       int32_t out_dtype, mla_stream_t stream);
 
 /*
  * mla_verify_attn_noalloc -- mla_verify_attn for callers that cannot allocate

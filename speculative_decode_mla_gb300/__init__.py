@@ -19,7 +19,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmla_verify.so")
 
 MLA_OK = 0
-MLA_DTYPE_BF16, MLA_DTYPE_F32 = 0, 1
+MLA_DTYPE_BF16, MLA_DTYPE_F32, MLA_DTYPE_F16 = 0, 1, 2
 MLA_FLAG_DEBUG_CHECKS, MLA_FLAG_SIMT = 1, 2
 CHECK_BAD_SLOT, CHECK_BAD_PARENT, CHECK_BAD_LENGTH, CHECK_TIMEOUT = 1, 2, 4, 8
 D_LATENT, D_ROPE = 512, 64
@@ -64,7 +64,7 @@ def load_library(path: str = LIB_PATH):
     lib.mla_verify_plan.argtypes = [ctypes.POINTER(Desc), i32, ctypes.POINTER(Plan)]
     lib.mla_verify_workspace_size.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(ctypes.c_size_t)]
     lib.mla_verify_attn.argtypes = [ctypes.POINTER(Desc), P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
-    lib.mla_verify_combine.argtypes = [i32, i64, i32, P, P, P, P, i32, P]
+    lib.mla_verify_combine.argtypes = [i32, i64, i32, P, i32, P, P, P, i32, P]
     lib.mla_verify_status_string.argtypes = [ctypes.c_int]
     lib.mla_verify_status_string.restype = ctypes.c_char_p
     lib.mla_fill_normal_bf16.argtypes = [P, i64, ctypes.c_uint64, ctypes.c_uint64, P]
@@ -154,7 +154,7 @@ def verify(q, kv_pool, slot_table, seq_lens, tree_parent, *, max_seq_len: int,
 
 
 def combine(part_o, part_lse, *, out_dtype: int = MLA_DTYPE_BF16, out=None, lse=None, stream=None):
-    """LSE-weighted merge of partials: part_o f32 [S, rows, d_v], part_lse f32 [S, rows]."""
+    """LSE-weighted merge of partials: part_o f32 or f16 [S, rows, d_v], part_lse f32 [S, rows]."""
     import torch
     S, rows, d_v = part_o.shape
     if out is None:
@@ -162,8 +162,11 @@ def combine(part_o, part_lse, *, out_dtype: int = MLA_DTYPE_BF16, out=None, lse=
                           dtype=torch.bfloat16 if out_dtype == MLA_DTYPE_BF16 else torch.float32)
     if lse is None:
         lse = torch.empty((rows,), device=part_o.device, dtype=torch.float32)
-    rc = load_library().mla_verify_combine(S, rows, d_v, part_o.data_ptr(), part_lse.data_ptr(), out.data_ptr(),
-                                           lse.data_ptr(), out_dtype, _stream_ptr(stream))
+    part_dtype = MLA_DTYPE_F16 if part_o.dtype == torch.float16 else MLA_DTYPE_F32
+    if part_o.dtype not in (torch.float16, torch.float32):
+        raise ValueError("part_o must be float32 or float16")
+    rc = load_library().mla_verify_combine(S, rows, d_v, part_o.data_ptr(), part_dtype, part_lse.data_ptr(),
+                                           out.data_ptr(), lse.data_ptr(), out_dtype, _stream_ptr(stream))
     _check(rc, "mla_verify_combine")
     return out, lse
 

@@ -86,7 +86,7 @@ extern "C" int mla_verify_plan(const mla_verify_desc* d, int32_t num_sms, mla_ve
   const int64_t units = (int64_t)d->num_seqs * p.row_tiles * p.num_splits;
   p.ctas = (int32_t)(simt ? units : 2 * units);
   const int64_t rows = (int64_t)d->num_seqs * R;
-  const int64_t o_bytes = (int64_t)p.num_splits * rows * kDLatent * 4;
+  const int64_t o_bytes = (int64_t)p.num_splits * rows * kDLatent * 2;  // fp16 partials
   const int64_t l_bytes = (int64_t)p.num_splits * rows * 4;
   p.workspace_bytes = cdiv(o_bytes, 256) * 256 + cdiv(l_bytes, 256) * 256;
   *plan = p;
@@ -149,8 +149,8 @@ extern "C" int mla_verify_attn(const mla_verify_desc* d, const void* q, const vo
   a.slot_table = slot_table;
   a.seq_lens = seq_lens;
   a.tree_parent = tree_parent;
-  a.part_o = static_cast<float*>(workspace);
-  const int64_t o_bytes = (int64_t)p.num_splits * rows * kDLatent * 4;
+  a.part_o = static_cast<__half*>(workspace);
+  const int64_t o_bytes = (int64_t)p.num_splits * rows * kDLatent * 2;
   a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + cdiv(o_bytes, 256) * 256);
   a.dev_status = dev_status;
   a.num_slots = d->num_slots;
@@ -172,7 +172,8 @@ extern "C" int mla_verify_attn(const mla_verify_desc* d, const void* q, const vo
   if (debug && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess) return MLA_ERR_CUDA;
   cudaError_t e = p.kernel == 1 ? launch_verify_simt(a, s) : launch_verify_tc(a, s);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
-  e = launch_combine(p.num_splits, rows, kDLatent, a.part_o, a.part_lse, out, lse, d->out_dtype, s);
+  e = launch_combine(p.num_splits, rows, kDLatent, a.part_o, MLA_DTYPE_F16, a.part_lse, out, lse, d->out_dtype,
+                     /*dependent=*/true, s);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   if (debug) {
     int32_t h = 0;
@@ -183,17 +184,18 @@ extern "C" int mla_verify_attn(const mla_verify_desc* d, const void* q, const vo
   return MLA_OK;
 }
 
-extern "C" int mla_verify_combine(int32_t num_splits, int64_t rows, int32_t d_v, const float* part_o,
-                                  const float* part_lse, void* out, float* lse, int32_t out_dtype,
-                                  mla_stream_t stream) {
+extern "C" int mla_verify_combine(int32_t num_splits, int64_t rows, int32_t d_v, const void* part_o,
+                                  int32_t part_dtype, const float* part_lse, void* out, float* lse,
+                                  int32_t out_dtype, mla_stream_t stream) {
+  if (part_dtype != MLA_DTYPE_F32 && part_dtype != MLA_DTYPE_F16) return MLA_ERR_INVALID_ARGUMENT;
   if (num_splits < 1 || rows < 0 || d_v < 4 || d_v % 4 != 0 || d_v > 1024) return MLA_ERR_INVALID_ARGUMENT;
   if (rows > (1ll << 31) - 1) return MLA_ERR_UNSUPPORTED;
   if (out_dtype != MLA_DTYPE_BF16 && out_dtype != MLA_DTYPE_F32) return MLA_ERR_INVALID_ARGUMENT;
   if (rows > 0 && (!part_o || !part_lse || !out)) return MLA_ERR_INVALID_ARGUMENT;
   if (!aligned(part_o, 16) || !aligned(out, 16) || !aligned(part_lse, 4) || !aligned(lse, 4))
     return MLA_ERR_INVALID_ARGUMENT;
-  cudaError_t e = launch_combine(num_splits, rows, d_v, part_o, part_lse, out, lse, out_dtype,
-                                 reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_combine(num_splits, rows, d_v, part_o, part_dtype, part_lse, out, lse, out_dtype,
+                                 /*dependent=*/false, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -22,7 +23,7 @@ struct VerifyArgs {
   const int32_t* slot_table;
   const int32_t* seq_lens;
   const int32_t* tree_parent;
-  float* part_o;      // [splits][rows][512]
+  __half* part_o;     // [splits][rows][512] fp16, each split normalised over its own part
   float* part_lse;    // [splits][rows]
   int32_t* dev_status;
   int64_t num_slots;
@@ -37,8 +38,11 @@ struct VerifyArgs {
 // Host-side launchers (each returns a cudaError_t from the launch).
 cudaError_t launch_verify_simt(const VerifyArgs& a, cudaStream_t stream);
 cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream);
-cudaError_t launch_combine(int32_t splits, int64_t rows, int32_t d_v, const float* part_o,
-                           const float* part_lse, void* out, float* lse, int32_t out_dtype,
+// part_dtype: MLA_DTYPE_F32 or MLA_DTYPE_F16. With `dependent`, the launch may start while the
+// preceding kernel on the stream finishes (programmatic dependent launch); the kernel waits
+// for that kernel's results before reading the partials.
+cudaError_t launch_combine(int32_t splits, int64_t rows, int32_t d_v, const void* part_o, int32_t part_dtype,
+                           const float* part_lse, void* out, float* lse, int32_t out_dtype, bool dependent,
                            cudaStream_t stream);
 int tc_kernel_supported();
 

@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(kWarps * 32) verify_simt_kernel(VerifyArgs a) 
   const int64_t N = (int64_t)L + a.T;
   const int64_t t0 = (int64_t)s * a.chunk;
   const int64_t t1 = min(N, t0 + a.chunk);
-  float* po = a.part_o + ((int64_t)s * a.rows + row) * kDLatent;
+  __half* po = a.part_o + ((int64_t)s * a.rows + row) * kDLatent;
   if (t0 >= t1) {
     if (lane == 0) a.part_lse[(int64_t)s * a.rows + row] = -INFINITY;
     return;
@@ -82,9 +82,9 @@ __global__ void __launch_bounds__(kWarps * 32) verify_simt_kernel(VerifyArgs a) 
     return;
   }
   const float inv = 1.f / l;
-  float2* po2 = reinterpret_cast<float2*>(po);
+  __half2* po2 = reinterpret_cast<__half2*>(po);
 #pragma unroll
-  for (int j = 0; j < kValPairsPerLane; ++j) po2[lane + 32 * j] = make_float2(o[j].x * inv, o[j].y * inv);
+  for (int j = 0; j < kValPairsPerLane; ++j) po2[lane + 32 * j] = __floats2half2_rn(o[j].x * inv, o[j].y * inv);
   if (lane == 0) a.part_lse[(int64_t)s * a.rows + row] = m + logf(l);
 }
 

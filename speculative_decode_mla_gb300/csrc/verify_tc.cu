@@ -27,9 +27,10 @@
 //                       domain (O is rescaled only when the running max grows by more
 //                       than 2^8), write P (bf16) to TMEM.
 //   release warp 5      tells the partner when this CTA has read a score buffer.
-//   epilogue            O_r / l goes through 128B-swizzled smem to TMA tensor stores
-//                       (rows past the sequence are clipped by the tensor map); lse to
-//                       the split workspace. The combine kernel merges the splits.
+//   epilogue            O_r / l (fp16) goes through 128B-swizzled smem to TMA tensor
+//                       stores (rows past the sequence are clipped by the tensor map); lse
+//                       to the split workspace. The combine kernel, launched as a
+//                       programmatic dependent, merges the splits.
 //
 // Every wait is bounded (about 2 s); on timeout the kernel stops issuing work,
 // drains what it started, reports MLA_CHECK_TIMEOUT in dev_status when given,
@@ -52,7 +53,7 @@ constexpr int kXBytes = kXHalfBytes + kRows * 4;    // + one fp32 reference per 
 constexpr int kSmemX = kStages * kStageBytes;       // two exchange buffers follow the stages
 constexpr int kSmemBar = kSmemX + 2 * kXBytes;
 constexpr int kSmemBytes = kSmemBar + 512 + 1024;   // barriers, TMEM slot, tree parents + alignment slack
-constexpr int kEpiBoxBytes = kRows * 128;           // one 32-column fp32 box of O (reuses the stages)
+constexpr int kEpiBoxBytes = kRows * 128;           // one 64-column fp16 box of O (reuses the stages)
 
 constexpr int kProducerWarps = kStages;
 constexpr int kMmaWarp = 4;
@@ -243,6 +244,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) TRACE(0);
+  // Let the dependent combine grid be scheduled early; it waits for this grid's results anyway.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   uint32_t rank;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
   const uint32_t peer = rank ^ 1u;
@@ -667,16 +670,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv = l_bf > 0.f ? 1.f / l_bf : 0.f;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {  // box c holds columns [32c, 32c + 32) of this CTA's half
-        uint32_t o[32];
-        TMEM_LD16(lane_addr + kColO + c * 32, o);
-        TMEM_LD16(lane_addr + kColO + c * 32 + 16, (o + 16));
-        tmem_wait_ld();
-        float4* box = reinterpret_cast<float4*>(smem + c * kEpiBoxBytes + r * 128);
+      for (int c = 0; c < 4; ++c) {  // box c holds columns [64c, 64c + 64) of this CTA's half, fp16
+        uint32_t o[64];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          box[u ^ (r & 7)] = make_float4(__uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
-                                         __uint_as_float(o[4 * u + 2]) * inv, __uint_as_float(o[4 * u + 3]) * inv);
+        for (int u = 0; u < 4; ++u) TMEM_LD16(lane_addr + kColO + c * 64 + u * 16, (o + u * 16));
+        tmem_wait_ld();
+        uint4* box = reinterpret_cast<uint4*>(smem + c * kEpiBoxBytes + r * 128);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {  // 16-byte chunk u = 8 columns, at position u ^ (r & 7)
+          uint32_t w[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const __half2 h = __floats2half2_rn(__uint_as_float(o[8 * u + 2 * k]) * inv,
+                                                __uint_as_float(o[8 * u + 2 * k + 1]) * inv);
+            w[k] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+          box[u ^ (r & 7)] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
       }
       fence_proxy_async();
       __syncwarp();
@@ -686,10 +696,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (ok && lane == 0) {
           const int z = s * a.B + b;
 #pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 0; c < 4; ++c) {
             asm volatile(
                 "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(&tmap_o),
-                "r"((int)rank * 256 + c * 32), "r"(row0), "r"(z), "r"(base + c * kEpiBoxBytes)
+                "r"((int)rank * 256 + c * 64), "r"(row0), "r"(z), "r"(base + c * kEpiBoxBytes)
                 : "memory");
           }
           asm volatile("cp.async.bulk.commit_group;" ::: "memory");
@@ -758,17 +768,17 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream) {
   }
   const int64_t units = (int64_t)a.B * a.row_tiles * a.splits;
   if (units * 2 > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  // The split partials viewed as [splits * B][R][512] fp32; a store box is 32 columns x 128 rows,
+  // The split partials viewed as [splits * B][R][512] fp16; a store box is 64 columns x 128 rows,
   // so rows past a sequence's R rows fall outside dimension 1 and are not written.
   const int R = a.T * a.H;
   CUtensorMap tmap;
   const cuuint64_t dims[3] = {(cuuint64_t)kDLatent, (cuuint64_t)R, (cuuint64_t)a.splits * (cuuint64_t)a.B};
-  const cuuint64_t strides[2] = {(cuuint64_t)kDLatent * 4, (cuuint64_t)R * kDLatent * 4};
-  const cuuint32_t box[3] = {32, (cuuint32_t)kRows, 1};
+  const cuuint64_t strides[2] = {(cuuint64_t)kDLatent * 2, (cuuint64_t)R * kDLatent * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kRows, 1};
   const cuuint32_t elem[3] = {1, 1, 1};
   EncodeTiledFn enc = encode_tiled();
   if (enc == nullptr) return cudaErrorNotSupported;
-  if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.part_o, dims, strides, box, elem,
+  if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.part_o, dims, strides, box, elem,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;

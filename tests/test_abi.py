@@ -58,7 +58,7 @@ def test_plan_64k_fills_the_gpu(lib):
     assert p.chunk_tokens % 64 == 0
     assert p.num_splits * p.chunk_tokens >= 65552 > (p.num_splits - 1) * p.chunk_tokens
     assert 60 <= p.num_splits <= 76 and p.ctas == 2 * p.num_splits
-    assert p.workspace_bytes >= p.num_splits * 128 * 512 * 4 + p.num_splits * 128 * 4
+    assert p.workspace_bytes >= p.num_splits * 128 * 512 * 2 + p.num_splits * 128 * 4
 
 
 def test_plan_forced_splits_and_simt(lib):
@@ -110,10 +110,11 @@ def test_attn_rejects_null_and_misaligned_pointers(lib):
 
 def test_combine_rejects_bad_args(lib):
     f = lib.mla_verify_combine
-    assert f(0, 4, 512, 16, 16, 16, 16, 0, None) == -1      # no splits
-    assert f(2, 4, 510, 16, 16, 16, 16, 0, None) == -1      # d_v not a multiple of 4
-    assert f(2, 4, 512, 16, 16, 16, 16, 5, None) == -1      # bad dtype
-    assert f(2, 4, 512, 0, 16, 16, 16, 0, None) == -1       # null partials
+    assert f(0, 4, 512, 16, 1, 16, 16, 16, 0, None) == -1      # no splits
+    assert f(2, 4, 510, 16, 1, 16, 16, 16, 0, None) == -1      # d_v not a multiple of 4
+    assert f(2, 4, 512, 16, 1, 16, 16, 16, 5, None) == -1      # bad output dtype
+    assert f(2, 4, 512, 16, 0, 16, 16, 16, 0, None) == -1      # partials must be f32 or f16
+    assert f(2, 4, 512, 0, 1, 16, 16, 16, 0, None) == -1       # null partials
 
 
 def test_status_strings(lib):

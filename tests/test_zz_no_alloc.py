@@ -82,10 +82,8 @@ def test_noalloc_matches_workspace_entry_point_twice(lib):
 def test_noalloc_rejects_problems_beyond_its_scratch(lib):
     import torch
     import speculative_decode_mla_gb300 as m
-    # the wide workload (64 nodes x 64 heads over 131k positions) needs more than 32 MiB of partials
-    cfg = W.CONFIGS["wide"]
-    desc = m.make_desc(1, cfg.num_nodes, cfg.num_heads, cfg.pool_slots, cfg.prefix_len + cfg.num_nodes,
-                       cfg.prefix_len)
+    # 16 sequences of 64 nodes x 64 heads over 131k positions need more than 32 MiB of partials
+    desc = m.make_desc(16, 64, 64, 1 << 24, 131072 + 64, 131072)
     assert m.workspace_size(desc) > SCRATCH_BYTES
     out = torch.zeros(16, dtype=torch.float32, device="cuda")
     fake = out.data_ptr()

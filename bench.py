@@ -130,6 +130,11 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# the files the tcgen05 attention kernel is built from (with the headers): the ncu traffic
+# record below is only used while they are unchanged
+TC_SOURCES = ["verify_tc.cu", "common.cuh"]
+
+
 def traffic_record(fingerprint):
     """dram read+write bytes of the attention kernel from the committed ncu summary, if it is current."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -329,8 +334,7 @@ def run_gpu(args):
     pk, pk_kind = peaks()
     peak_hbm = float(pk["hbm_gbs"])
     achieved = alg_bytes / attn_s / 1e9
-    fp = open(_build.LIB + ".fingerprint").read() if os.path.exists(_build.LIB + ".fingerprint") else None
-    traffic = traffic_record(fp)
+    traffic = traffic_record(_build.source_fingerprint(TC_SOURCES)) if plan.kernel == 0 else None
     launches = 2 * args.steps  # attention kernel + combine kernel per step
 
     base = None

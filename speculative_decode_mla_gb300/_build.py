@@ -27,15 +27,25 @@ def _sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _fingerprint() -> str:
+def source_fingerprint(names=None) -> str:
+    """Hash of the compile flags and of the named csrc files (all sources when None) plus every
+    header, by file name and contents, so it is the same wherever the tree is checked out."""
     h = hashlib.sha256()
-    h.update(" ".join(FLAGS).encode())
-    files = _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + sorted(glob.glob(os.path.join(INCLUDE, "*.h")))
+    h.update(" ".join(f for f in FLAGS if not os.path.isabs(f)).encode())
+    if names is None:
+        files = _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh")))
+    else:
+        files = [os.path.join(CSRC, n) for n in names]
+    files += sorted(glob.glob(os.path.join(INCLUDE, "*.h")))
     for f in files:
-        h.update(f.encode())
+        h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
+
+
+def _fingerprint() -> str:
+    return source_fingerprint()
 
 
 def build(force: bool = False, verbose: bool = False) -> str:

@@ -6,27 +6,29 @@
 // [512 + 32r, 512 + 32r + 32) of every 576-dim latent row. Per 64-position tile:
 //
 //   producer warps 0-3  gather: slot = slot_table[b][t] (page_size=1), then 16-byte
-//                       cp.async of this CTA's 512 value bytes and the 128-byte RoPE
-//                       block of row kv[slot] into a 128B-swizzled (UMMA K-major)
-//                       smem stage. Warp p owns stage p and tiles p, p+4, ...; it marks
-//                       a tile ready as soon as its own copies have landed.
-//   MMA warp 4          S_r = Q_r K_r^T over the CTA's 288 contraction dims
-//                       (tcgen05.mma kind::f16, A = Q from TMEM, B = K from smem, fp32
-//                       accumulate in TMEM); O_r += P V_r (A = P from TMEM, B = the same K
-//                       stage read MN-major, N = 256). An event loop issues whichever of S
-//                       and PV is ready, so neither waits on the other.
-//   sender warps 10-13  as soon as S_r is in TMEM, push it to the partner CTA through
+//                       cp.async of this CTA's 512 value bytes (128B-swizzled, UMMA K-major)
+//                       and its 64 RoPE bytes (64B-swizzled) of row kv[slot] into a smem
+//                       stage. Warp p takes rows 16p..16p+15 of every tile and the tiles go
+//                       out in order; a stage's barrier fires when its copies land
+//                       (cp.async.mbarrier.arrive.noinc), so no producer waits on its own
+//                       copies. One producer per warp scheduler keeps the issue load even.
+//   S issuer warp 4     S_r(t) = Q_r K_r^T over the CTA's 288 contraction dims into the TMEM
+//                       score buffer (tcgen05.mma kind::f16, fp32 accumulate; A = Q from
+//                       TMEM, B = K from the stage) once the softmax and the sender have
+//                       read S_r(t-1).
+//   PV issuer warp 5    O_r += P(t) V_r(t) (A = P from TMEM, B = the same stage read
+//                       MN-major, N = 256); its completion frees the stage.
+//   sender warps 11-14  as soon as S_r(t) is in TMEM, push it to the partner CTA through
 //                       distributed shared memory (st.async with a byte count on the
-//                       partner's mbarrier; two receive buffers per CTA). The partner's
-//                       partial travels in the exp2 domain as fp16 offsets from a per-row
-//                       fp32 reference (the row's largest partial in the tile): half the
-//                       bytes of fp32, most precise for the keys that carry the weight.
-//   softmax warps 6-9   one thread per query row: read S_r from TMEM, add the partner's
-//                       partial (S = S_0 + S_1), apply the
-//                       ancestor bitmask on tree positions, online softmax in the exp2
-//                       domain (O is rescaled only when the running max grows by more
-//                       than 2^8), write P (bf16) to TMEM.
-//   release warp 5      tells the partner when this CTA has read a score buffer.
+//                       partner's mbarrier; two receive buffers per CTA). The partial
+//                       travels in the exp2 domain as fp16 offsets from a per-row fp32
+//                       reference (the row's largest visible partial in the tile).
+//   softmax warps 7-10  one thread per query row: read S_r(t) from TMEM, add the partner's
+//                       partial (S = S_0 + S_1), apply the ancestor bitmask on tree
+//                       positions, online softmax in the exp2 domain (O is rescaled only
+//                       when the running max grows by more than 2^8), write P (bf16) to
+//                       TMEM.
+//   release warp 6      tells the partner when this CTA has read a receive buffer.
 //   epilogue            O_r / l (fp16) goes through 128B-swizzled smem to TMA tensor
 //                       stores (rows past the sequence are clipped by the tensor map); lse
 //                       to the split workspace. The combine kernel, launched as a
@@ -45,30 +47,37 @@ namespace {
 
 constexpr int kRows = 128;              // query rows per tile (MMA M)
 constexpr int kKeys = 64;               // positions per KV tile (S MMA N)
-constexpr int kStages = 4;  // one per producer warp
-constexpr int kBlockBytes = kKeys * 128;            // 64 rows x 128 B (one 64-dim block)
-constexpr int kStageBytes = 5 * kBlockBytes;        // 4 value blocks + the RoPE block
+constexpr int kStages = 4;              // KV stages in shared memory
+constexpr int kBlockBytes = kKeys * 128;            // 64 rows x 128 B (one 64-dim block, 128B swizzle)
+constexpr int kRopeBytes = kKeys * 64;              // 64 rows x 64 B: this CTA's 32 RoPE dims, 64B swizzle
+constexpr int kStageBytes = 4 * kBlockBytes + kRopeBytes;  // 4 value blocks + the RoPE half
 constexpr int kXHalfBytes = kRows * kKeys * 2;      // fp16 partial scores of one tile
 constexpr int kXBytes = kXHalfBytes + kRows * 4;    // + one fp32 reference per row
 constexpr int kSmemX = kStages * kStageBytes;       // two exchange buffers follow the stages
 constexpr int kSmemBar = kSmemX + 2 * kXBytes;
 constexpr int kSmemBytes = kSmemBar + 512 + 1024;   // barriers, TMEM slot, tree parents + alignment slack
 constexpr int kEpiBoxBytes = kRows * 128;           // one 64-column fp16 box of O (reuses the stages)
+static_assert(kStageBytes % 1024 == 0 && kSmemX % 16 == 0, "stage and exchange alignment");
+static_assert(kSmemBytes <= 232448, "shared memory");
 
-constexpr int kProducerWarps = kStages;
-constexpr int kMmaWarp = 4;
-constexpr int kReleaseWarp = 5;
-constexpr int kSoftmaxWarp0 = 6;  // warps 6..9: TMEM lane quarters 2, 3, 0, 1
-constexpr int kSenderWarp0 = 10;  // warps 10..13: TMEM lane quarters 2, 3, 0, 1
-constexpr int kThreads = 14 * 32;
+constexpr int kProducerWarps = 4;  // warps 0..3, one per scheduler; warp p gathers rows 16p..16p+15 of each tile
+constexpr int kSIssueWarp = 4;      // issues S = Q K^T; allocates and frees TMEM
+constexpr int kPVIssueWarp = 5;     // issues O += P V
+constexpr int kReleaseWarp = 6;     // tells the partner when a receive buffer has been read
+constexpr int kSoftmaxWarp0 = 7;    // warps 7..10: TMEM lane quarters 3, 0, 1, 2
+constexpr int kSenderWarp0 = 11;    // warps 11..14: TMEM lane quarters 3, 0, 1, 2
+constexpr int kThreads = 15 * 32;
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;  // O 256, S 64, P 32, Q 144 columns
 
 // barrier indices (8 bytes each)
-constexpr int kBarKvFull = 0, kBarKvEmpty = 4, kBarQFull = 8, kBarSFull = 9, kBarSEmpty = 10, kBarPFull = 11,
-              kBarPEmpty = 12, kBarXFull = 13 /*2*/, kBarXEmpty = 15 /*2*/, kBarXRead = 17 /*2*/, kBarDrain = 19,
-              kBarEpi = 20, kNumBars = 21;
+constexpr int kBarKvFull = 0, kBarKvEmpty = kStages, kBarQFull = 2 * kStages, kBarSFull = kBarQFull + 1,
+              kBarSEmpty = kBarQFull + 2, kBarPFull = kBarQFull + 3, kBarPEmpty = kBarQFull + 4,
+              kBarXFull = kBarQFull + 5 /*2*/, kBarXEmpty = kBarQFull + 7 /*2*/, kBarXRead = kBarQFull + 9 /*2*/,
+              kBarDrainS = kBarQFull + 11, kBarDrainP = kBarQFull + 12, kBarEpi = kBarQFull + 13,
+              kNumBars = kBarQFull + 14;
+static_assert(8 * kNumBars + 8 + 4 * kMaxNodes <= 512, "barrier area");
 
 constexpr long long kTimeoutCycles = 4000000000ll;  // ~2 s at 2 GHz
 
@@ -126,16 +135,6 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
       : "memory");
   return ok != 0;
 }
-// Non-blocking probe of a phase (for the MMA issuer's event loop).
-__device__ __forceinline__ bool mbar_probe(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 // Bounded wait: false when another role aborted or the wait timed out (then it aborts).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                          bool cluster_scope = false) {
@@ -163,11 +162,7 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t cta) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -258,11 +253,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int b = bt / a.row_tiles;
   const int R = a.T * a.H;
   const int row0 = tile_idx * kRows;
-  const int32_t L = load_len(a, b);
-  const int64_t N = (int64_t)L + a.T;
   const int64_t t0 = (int64_t)s * a.chunk;
+
+  // The reads the set-up waits on are issued together, before anything waits on one: the slots
+  // of the first kStages tiles (producer warp), the prefix length and the tree parents. The query
+  // rows are read after the set-up, so they do not delay it.
+  const int32_t* tab = a.slot_table + (int64_t)b * a.stride;
+  int32_t sr[kStages];  // producer warp p, lane l: slot of row 16p + (l & 15) of each of the next kStages tiles
+  const bool producer = warp < kProducerWarps;
+  if (producer) {
+    const int64_t pre_end = min(t0 + (int64_t)a.chunk, (int64_t)a.stride);  // stays inside this row
+#pragma unroll
+    for (int j = 0; j < kStages; ++j) {
+      const int64_t pos = t0 + (int64_t)j * kKeys + warp * 16 + (lane & 15);
+      sr[j] = pos < pre_end ? tab[pos] : 0;
+    }
+  }
+  const int32_t L_raw = a.seq_lens[b];
+  const int32_t par_raw = threadIdx.x < a.T ? a.tree_parent[(int64_t)b * a.T + threadIdx.x] : -1;
+
+  int32_t L = L_raw;
+  if (L < 0 || L > a.max_seq_len) {
+    report(a.dev_status, a.debug, MLA_CHECK_BAD_LENGTH);
+    L = L < 0 ? 0 : a.max_seq_len;
+  }
+  const int64_t N = (int64_t)L + a.T;
   const int64_t t1 = min(N, t0 + a.chunk);
-  if (t0 >= t1) {  // nothing of this sequence falls in this chunk: an empty partial
+  if (t0 >= t1) {  // nothing of this sequence falls in this chunk: an empty partial (both CTAs agree)
     if (rank == 0 && threadIdx.x < kRows && row0 + (int)threadIdx.x < R)
       a.part_lse[(int64_t)s * a.rows + (int64_t)b * R + row0 + threadIdx.x] = -INFINITY;
     return;
@@ -271,20 +288,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(bar(kBarKvFull + i), 32);  // the owning producer warp
+      mbar_init(bar(kBarKvFull + i), 32 * kProducerWarps);  // one asynchronous arrive per producer lane
       mbar_init(bar(kBarKvEmpty + i), 1);
     }
-    mbar_init(bar(kBarQFull), 4);
+    mbar_init(bar(kBarQFull), 8);  // the softmax and the sender warps each stored their Q chunks
     mbar_init(bar(kBarSFull), 1);
     mbar_init(bar(kBarSEmpty), 8);  // the softmax and the sender warps have both read S
-    mbar_init(bar(kBarPFull), 4);
-    mbar_init(bar(kBarPEmpty), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarXFull + i), 1);   // armed locally with the exchange's byte count
-      mbar_init(bar(kBarXEmpty + i), 1);  // one remote arrive per use from the partner
+      mbar_init(bar(kBarXEmpty + i), 1);  // one remote arrive from the partner's release warp per use
       mbar_init(bar(kBarXRead + i), 4);   // the four softmax warps have read the buffer
     }
-    mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarPFull), 4);
+    mbar_init(bar(kBarPEmpty), 1);
+    mbar_init(bar(kBarDrainS), 1);
+    mbar_init(bar(kBarDrainP), 1);
     mbar_init(bar(kBarEpi), 4);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -292,144 +310,200 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_arrive_expect_tx(bar(kBarXFull + 1), kXBytes);
   }
   if (threadIdx.x < a.T) {  // tree parents of this sequence, validated, into shared memory
-    int p = a.tree_parent[(int64_t)b * a.T + threadIdx.x];
+    int p = par_raw;
     if (p < -1 || p >= (int)threadIdx.x) {
       report(a.dev_status, a.debug, MLA_CHECK_BAD_PARENT);
       p = -1;
     }
     s_parent[threadIdx.x] = p;
   }
-  if (warp == kMmaWarp) {
+  if (warp == kSIssueWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  cluster_sync();  // barrier inits visible to the partner before any remote operation
-  const uint32_t tmem = *tmem_slot;
+  // The producer warps only signal that the barriers and parents they wrote are ready (named
+  // barrier 1, and their arrival on the cluster barrier) and start the KV stream at once; they
+  // need neither TMEM nor the partner, and complete their cluster-barrier phase after their last
+  // copy. Named barrier 2 makes thread 0's barrier inits visible to the other producer warps.
+  uint32_t tmem = 0;
+  if (producer) {
+    asm volatile("bar.sync 2, %0;" ::"n"(32 * kProducerWarps) : "memory");
+    asm volatile("bar.arrive 1, %0;" ::"n"(kThreads) : "memory");
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  } else {
+    tc_fence_before();
+    asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+    tc_fence_after();
+    cluster_sync();  // barrier inits visible to the partner before any remote operation
+    tmem = *tmem_slot;
+  }
   if (threadIdx.x == 0) TRACE(1);
 
-  if (warp < kProducerWarps) {
-    // ---------------------------------------------------------------- producer: page_size=1 gather
-    const int stage = warp;
-    const uint32_t sbase = base + stage * kStageBytes;
-    const char* kvb = reinterpret_cast<const char*>(a.kv);
-    const int32_t* tab = a.slot_table + (int64_t)b * a.stride;
-    // lane l fetches the slots of positions l and l + 32 of a tile; positions past the end
-    // read row 0 (masked later). The next tile's slots are fetched while this one loads.
-    auto fetch = [&](int t, int k) -> int32_t {
-      const int64_t pos = t0 + (int64_t)t * kKeys + k;
-      return (t < ntiles && pos < t1) ? tab[pos] : 0;
-    };
-    int32_t next0 = fetch(warp, lane), next1 = fetch(warp, lane + 32);
-    for (int t = warp; t < ntiles; t += kProducerWarps) {
-      if (t >= kStages && !wait_warp(bar(kBarKvEmpty + stage), ((t / kStages) - 1) & 1, abort_flag)) break;
-      int32_t s0 = next0, s1 = next1;
-      next0 = fetch(t + kProducerWarps, lane);
-      next1 = fetch(t + kProducerWarps, lane + 32);
-      if (s0 < 0 || (int64_t)s0 >= a.num_slots || s1 < 0 || (int64_t)s1 >= a.num_slots) {
-        report(a.dev_status, a.debug, MLA_CHECK_BAD_SLOT);
-        s0 = s0 < 0 ? 0 : (int32_t)min((int64_t)s0, a.num_slots - 1);
-        s1 = s1 < 0 ? 0 : (int32_t)min((int64_t)s1, a.num_slots - 1);
-      }
-#pragma unroll 8
-      for (int k = 0; k < kKeys; ++k) {  // this CTA's 512 value bytes of one row per instruction
-        const int64_t sl = __shfl_sync(0xffffffffu, k < 32 ? s0 : s1, k & 31);
-        const char* src = kvb + sl * (kDK * 2) + rank * 512 + lane * 16;
-        const uint32_t dst =
-            sbase + (lane >> 3) * kBlockBytes + k * 128 + ((((uint32_t)lane & 7u) ^ ((uint32_t)k & 7u)) << 4);
-        cp_async16(dst, src);
-      }
+  if (warp >= kSoftmaxWarp0) {
+    // Q -> TMEM, two bf16 per column: chunk c of the CTA's 36 (32 value, 4 RoPE) at column
+    // kColQ + 4c; the softmax warps store chunks 0-19, the sender warps chunks 20-35.
+    const bool q_sender = warp >= kSenderWarp0;
+    const int q_row = (warp & 3) * 32 + lane;  // tile row = TMEM lane of this thread
+    const int q_c0 = q_sender ? 20 : 0, q_n = q_sender ? 16 : 20;
+    const bool qvalid = row0 + q_row < R;
+    const uint4* qrow = reinterpret_cast<const uint4*>(a.q + (qvalid ? (int64_t)b * R + row0 + q_row : 0) * kDK);
+    uint32_t qv[80];
 #pragma unroll
-      for (int g = 0; g < kKeys / 4; ++g) {  // the 128-byte RoPE block of four rows per instruction
-        const int k = g * 4 + (lane >> 3);
-        const int64_t sl = __shfl_sync(0xffffffffu, k < 32 ? s0 : s1, k & 31);
-        const char* src = kvb + sl * (kDK * 2) + 1024 + (lane & 7) * 16;
-        const uint32_t dst =
-            sbase + 4 * kBlockBytes + k * 128 + ((((uint32_t)lane & 7u) ^ ((uint32_t)k & 7u)) << 4);
-        cp_async16(dst, src);
+    for (int i = 0; i < 20; ++i) {
+      const int chunk = q_c0 + i;
+      uint4 x = make_uint4(0, 0, 0, 0);
+      if (qvalid && i < q_n) {
+        const int src = chunk < 32 ? (int)rank * 32 + chunk : 64 + (int)rank * 4 + (chunk - 32);
+        x = __ldg(qrow + src);
       }
-      cp_async_commit();
-      if (lane == 0 && t < 24) TRACE(14 + 10 * t);  // tile t's copies issued
-      cp_async_wait<0>();
-      fence_proxy_async();
-      mbar_arrive(bar(kBarKvFull + stage));
-      if (lane == 0 && t < 24) TRACE(15 + 10 * t);  // tile t marked ready
+      qv[i * 4 + 0] = x.x;
+      qv[i * 4 + 1] = x.y;
+      qv[i * 4 + 2] = x.z;
+      qv[i * 4 + 3] = x.w;
     }
-    cp_async_wait<0>();
-  } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------------- MMA issuer (one thread)
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    if (!q_sender) {
+#pragma unroll
+      for (int c = 0; c < 5; ++c) TMEM_ST16(lane_addr + kColQ + c * 16, (qv + c * 16));
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) TMEM_ST16(lane_addr + kColQ + 80 + c * 16, (qv + c * 16));
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(kBarQFull));
+    if (warp == kSoftmaxWarp0 && lane == 0) TRACE(6);
+  }
+
+  if (producer) {
+    // ---------------------------------------------------------------- producers: page_size=1 gather
+    // Every producer warp issues its 16 rows of each tile, tile by tile in order, so across the
+    // GPU the first tiles' rows are requested first. No wait on their own copies:
+    // cp.async.mbarrier.arrive.noinc makes each lane's arrival on the stage's barrier fire once
+    // that lane's copies so far have landed.
+    const char* kvb = reinterpret_cast<const char*>(a.kv);
+    const int row_base = warp * 16;
+#pragma unroll
+    for (int j = 0; j < kStages; ++j) {  // positions past the end read row 0 (masked later)
+      const int64_t pos = t0 + (int64_t)j * kKeys + row_base + (lane & 15);
+      if (pos >= t1) sr[j] = 0;
+    }
+    bool ok = true;
+    for (int tb = 0; tb < ntiles && ok; tb += kStages) {
+#pragma unroll
+      for (int j = 0; j < kStages; ++j) {
+        const int t = tb + j;
+        if (t >= ntiles) break;
+        const uint32_t sbase = base + j * kStageBytes;
+        if (t >= kStages && !wait_warp(bar(kBarKvEmpty + j), ((t / kStages) - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        int32_t sl_own = sr[j];
+        {  // the slot of this lane's row of tile t + kStages, needed once this stage comes round again
+          const int64_t pn = t0 + (int64_t)(t + kStages) * kKeys + row_base + (lane & 15);
+          sr[j] = pn < t1 ? tab[pn] : 0;
+        }
+        if (sl_own < 0 || (int64_t)sl_own >= a.num_slots) {
+          report(a.dev_status, a.debug, MLA_CHECK_BAD_SLOT);
+          sl_own = sl_own < 0 ? 0 : (int32_t)min((int64_t)sl_own, a.num_slots - 1);
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {  // this CTA's 512 value bytes of one row per instruction
+          const int row = row_base + k;
+          const int64_t sl = __shfl_sync(0xffffffffu, sl_own, k);
+          const char* src = kvb + sl * (kDK * 2) + rank * 512 + lane * 16;
+          const uint32_t dst =
+              sbase + (lane >> 3) * kBlockBytes + row * 128 + ((((uint32_t)lane & 7u) ^ ((uint32_t)row & 7u)) << 4);
+          cp_async16(dst, src);
+        }
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {  // this CTA's 64 RoPE bytes of eight rows per instruction
+          const int kr = g * 8 + (lane >> 2);
+          const int row = row_base + kr;
+          const int64_t sl = __shfl_sync(0xffffffffu, sl_own, kr);
+          const char* src = kvb + sl * (kDK * 2) + 1024 + rank * 64 + (lane & 3) * 16;
+          const uint32_t dst = sbase + 4 * kBlockBytes + row * 64 +
+                               ((((uint32_t)lane & 3u) ^ (((uint32_t)row >> 1) & 3u)) << 4);
+          cp_async16(dst, src);
+        }
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar(kBarKvFull + j)) : "memory");
+        if (warp == 0 && lane == 0 && t < 24) TRACE(14 + 10 * t);  // tile t's copies issued (warp 0)
+      }
+    }
+    cp_async_wait_all();  // no copy may still be in flight when the CTA exits
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");  // this warp's setup phase
+  } else if (warp == kSIssueWarp) {
+    // ---------------------------------------------------------------- S issuer (one thread)
+    // S(t) = Q_r K_r^T over the CTA's 288 contraction dims (A = Q from TMEM, B = K from the
+    // stage) once tile t has landed and both readers are done with S(t-1).
     if (lane == 0) {
       constexpr uint32_t idesc_s = instr_desc(kRows, kKeys, 0);
-      constexpr uint32_t idesc_pv = instr_desc(kRows, 256, 1);
       bool ok = wait_bar(bar(kBarQFull), 0, abort_flag);
       TRACE(4);
-      tc_fence_after();
-      // Event loop: S(t) needs tile t's stage and S(t-1) read out of TMEM; PV(t) needs S(t)
-      // issued and P(t) written. Whichever is ready goes first, so neither waits on the other.
-      int ns = 0, np = 0;
-      long long idle_since = clock64();
-      while (ok && np < ntiles) {
-        bool progressed = false;
-        if (ns < ntiles && mbar_probe(bar(kBarKvFull + ns % kStages), (ns / kStages) & 1) &&
-            (ns == 0 || mbar_probe(bar(kBarSEmpty), (ns - 1) & 1))) {
-          if (ns == 0) TRACE(5);
-          tc_fence_after();
-          const uint32_t sbase = base + (ns % kStages) * kStageBytes;
-          const uint32_t dS = tmem + kColS;
+      for (int t = 0; t < ntiles && ok; ++t) {
+        ok = wait_bar(bar(kBarKvFull + t % kStages), (t / kStages) & 1, abort_flag);
+        if (ok && t >= 1) ok = wait_bar(bar(kBarSEmpty), (t - 1) & 1, abort_flag);
+        if (!ok) break;
+        if (t == 0) TRACE(5);
+        // the stage was written by cp.async (generic proxy) and is read by the MMA (async proxy)
+        fence_proxy_async();
+        tc_fence_after();
+        const uint32_t sbase = base + (t % kStages) * kStageBytes;
+        const uint32_t dS = tmem + kColS;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t bd = smem_desc(sbase + j * kBlockBytes + kk * 32, 16, 1024);
-              mma_tmem_a(dS, tmem + kColQ + j * 32 + kk * 8, bd, idesc_s, (j | kk) ? 1u : 0u);
-            }
-          }
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {  // this CTA's half of the RoPE dims
-            const uint64_t bd = smem_desc(sbase + 4 * kBlockBytes + (rank * 2 + kk) * 32, 16, 1024);
-            mma_tmem_a(dS, tmem + kColQ + 128 + kk * 8, bd, idesc_s, 1u);
-          }
-          mma_commit(bar(kBarSFull));
-          if (ns < 24) TRACE(16 + 10 * ns);  // S(ns) issued
-          ++ns;
-          progressed = true;
+        for (int i = 0; i < 16; ++i) {
+          const uint64_t bd = smem_desc(sbase + (i >> 2) * kBlockBytes + (i & 3) * 32, 16, 1024);
+          mma_tmem_a(dS, tmem + kColQ + i * 8, bd, idesc_s, i ? 1u : 0u);
         }
-        if (np < ns && mbar_probe(bar(kBarPFull), np & 1)) {
-          tc_fence_after();
-          const uint32_t sbase = base + (np % kStages) * kStageBytes;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {  // 16 positions per step; V read MN-major from the same stage
-            const uint64_t bd = smem_desc(sbase + kk * 2048, kBlockBytes, 1024);
-            mma_tmem_a(tmem + kColO, tmem + kColP + kk * 8, bd, idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(bar(kBarKvEmpty + np % kStages));
-          mma_commit(bar(kBarPEmpty));
-          if (np < 24) TRACE(17 + 10 * np);  // PV(np) issued
-          ++np;
-          progressed = true;
+        for (int kk = 0; kk < 2; ++kk) {  // this CTA's half of the RoPE dims (64B-swizzled, 512 B per 8 rows)
+          const uint64_t bd = smem_desc(sbase + 4 * kBlockBytes + kk * 32, 16, 512, 4);
+          mma_tmem_a(dS, tmem + kColQ + 128 + kk * 8, bd, idesc_s, 1u);
         }
-        if (progressed) {
-          idle_since = clock64();
-        } else if (*abort_flag) {
-          ok = false;
-        } else if (clock64() - idle_since > kTimeoutCycles) {
-          *abort_flag = 1;
-          ok = false;
-        }
+        mma_commit(bar(kBarSFull));
+        if (t < 24) TRACE(16 + 10 * t);  // S(t) issued
       }
-      // drain: every MMA issued so far has completed once this barrier flips
-      mma_commit(bar(kBarDrain));
+      // drain: every MMA this thread issued has completed once this barrier flips
+      mma_commit(bar(kBarDrainS));
       const long long st = clock64();
-      while (!mbar_test(bar(kBarDrain), 0) && clock64() - st < kTimeoutCycles) {
+      while (!mbar_test(bar(kBarDrainS), 0) && clock64() - st < kTimeoutCycles) {
+      }
+    }
+    __syncwarp();
+  } else if (warp == kPVIssueWarp) {
+    // ---------------------------------------------------------------- PV issuer (one thread)
+    // O_r += P(t) V_r(t) once the softmax has written P(t); its completion frees the KV stage
+    // and the P columns.
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = instr_desc(kRows, 256, 1);
+      bool ok = true;
+      for (int t = 0; t < ntiles && ok; ++t) {
+        ok = wait_bar(bar(kBarPFull), t & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sbase = base + (t % kStages) * kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {  // 16 positions per step; V read MN-major from the same stage
+          const uint64_t bd = smem_desc(sbase + kk * 2048, kBlockBytes, 1024);
+          mma_tmem_a(tmem + kColO, tmem + kColP + kk * 8, bd, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(kBarKvEmpty + t % kStages));
+        mma_commit(bar(kBarPEmpty));
+        if (t < 24) TRACE(17 + 10 * t);  // PV(t) issued
+      }
+      mma_commit(bar(kBarDrainP));
+      const long long st = clock64();
+      while (!mbar_test(bar(kBarDrainP), 0) && clock64() - st < kTimeoutCycles) {
       }
     }
     __syncwarp();
   } else if (warp == kReleaseWarp) {
-    // ---------------------------------------------------------------- score-buffer release to the partner
+    // ---------------------------------------------------------------- receive-buffer release to the partner
+    // (kept off the softmax warps: a cluster-scope release arrive is slow)
     if (lane == 0) {
       const uint32_t xempty_remote0 = map_to_cta(bar(kBarXEmpty), peer);
       for (int t = 0; t < ntiles; ++t) {
@@ -485,7 +559,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                             fmaf(__uint_as_float(su[k + 1]), a.scale_log2, -ref));
         hv[k / 2] = *reinterpret_cast<const uint32_t*>(&h);
       }
-      // the partner's buffer xb is free once it has read what this CTA sent two tiles ago
+      // the partner's buffer xb is free once it has read what this CTA sent there two tiles ago
       if (t >= 2 && !wait_warp(bar(kBarXEmpty + xb), ((t - 2) >> 1) & 1, abort_flag, true)) break;
       const uint32_t xr = x_remote0 + (uint32_t)(xb * kXBytes);
       const uint32_t xf = xfull_remote0 + 8u * (uint32_t)xb;
@@ -513,35 +587,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int64_t grow = (int64_t)b * R + local_row;
     const int node = valid ? local_row / a.H : 0;
 
-    // Q -> TMEM: this CTA's 256 value dims then its 32 RoPE dims, two bf16 per column.
-    // The loads of each half are issued before its TMEM stores so their latencies overlap.
-    const bool q_ok = true;
-    {
-      const uint4* qrow = reinterpret_cast<const uint4*>(a.q + (valid ? grow : 0) * kDK);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {  // 16-byte chunks [0, 20) then [20, 36): 0..31 value, 32..35 RoPE
-        const int c0 = half * 20, nc = half ? 16 : 20;
-        uint32_t v[80];
-#pragma unroll
-        for (int i = 0; i < nc; ++i) {
-          const int chunk = c0 + i;
-          const int src = chunk < 32 ? rank * 32 + chunk : 64 + rank * 4 + (chunk - 32);
-          const uint4 x = valid ? __ldg(qrow + src) : make_uint4(0, 0, 0, 0);
-          v[i * 4 + 0] = x.x;
-          v[i * 4 + 1] = x.y;
-          v[i * 4 + 2] = x.z;
-          v[i * 4 + 3] = x.w;
-        }
-#pragma unroll
-        for (int c = 0; c < nc / 4; ++c) TMEM_ST16(lane_addr + kColQ + (c0 / 4 + c) * 16, (v + c * 16));
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarQFull));
-      if (warp == kSoftmaxWarp0 && lane == 0) TRACE(6);
-    }
-
     // anc*(node) from the parents in shared memory: bit j set iff j is node or one of its ancestors
     uint64_t anc = ~0ull;
     if (valid) {
@@ -549,10 +594,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int j = node, step = 0; j >= 0 && step < kMaxNodes; j = s_parent[j], ++step) anc |= 1ull << j;
     }
 
-    // l_run sums the exact exponentials (for lse); l_bf sums the bf16-rounded P the MMA
-    // multiplies with (for normalising O, so a constant value column comes out as exactly 1)
-    float m_run = -INFINITY, l_run = 0.f, l_bf = 0.f;
-    bool ok = q_ok;
+    // l_run sums the exponentials (fp32, before P is rounded to bf16 for the MMA)
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
     for (int t = 0; t < ntiles && ok; ++t) {
       const int xb = t & 1;
       if (!wait_warp(bar(kBarSFull), t & 1, abort_flag)) { ok = false; break; }
@@ -593,7 +637,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarXRead + xb));  // the exchange warp releases it to the partner
+      if (lane == 0) mbar_arrive(bar(kBarXRead + xb));  // the release warp lets the partner refill it
+      if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(15 + 10 * t);
 
       // tree positions (tail tiles only) and positions past the end are masked
       const int64_t p0 = t0 + (int64_t)t * kKeys;
@@ -614,24 +659,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (m_new > m_run + 8.f) {  // also the first visible tile (m_run = -inf)
         alpha = ex2(m_run - m_new);
         l_run *= alpha;
-        l_bf *= alpha;
         m_run = m_new;
         rescale = t > 0;
       }
       const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
       uint32_t pk[kKeys / 2];
-      float lsum = 0.f, lbf = 0.f;
+      float lsum = 0.f;
 #pragma unroll
       for (int k = 0; k < kKeys; k += 2) {
         const float e0 = ex2(sc[k] + neg_m);
         const float e1 = ex2(sc[k + 1] + neg_m);
         const uint32_t pr = pack_bf16(e0, e1);
         lsum += e0 + e1;
-        lbf += __uint_as_float(pr << 16) + __uint_as_float(pr & 0xffff0000u);
         pk[k / 2] = pr;
       }
       l_run += lsum;
-      l_bf += lbf;
 
       // P -> TMEM once PV of the previous tile has finished with it (and with O)
       if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(12 + 10 * t);
@@ -668,7 +710,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == kSoftmaxWarp0 && lane == 0) TRACE(kTraceSlots - 4);
     if (ok) {
       tc_fence_after();
-      const float inv = l_bf > 0.f ? 1.f / l_bf : 0.f;
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {  // box c holds columns [64c, 64c + 64) of this CTA's half, fp16
         uint32_t o[64];
@@ -723,7 +765,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       a.part_lse[(int64_t)s * a.rows + (int64_t)b * R + row0 + threadIdx.x] = __int_as_float(0x7fc00000);
   }
   tc_fence_after();
-  if (warp == kMmaWarp) {
+  if (warp == kSIssueWarp) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
   cluster_sync();  // neither CTA leaves while the partner may still write into its shared memory

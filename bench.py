@@ -187,6 +187,56 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def measure_185k(m, W, dev, steps, warmup):
+    """The 185k full-depth step: 61 layers, each with its own device-drawn latent pool (about
+    13 GB together, far larger than L2) and query, one shared slot table. A step is the 61
+    mla_verify_attn calls, replayed from a CUDA graph; returns (s per step, kv bytes per layer, plan)."""
+    import torch
+    cfg = W.CONFIGS["185k"]
+    p0 = W.make_problem(cfg, layer=0, with_kv=False)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    st, sl, tp = t(p0.slot_table), t(p0.seq_lens), t(p0.tree_parent)
+    pools = torch.empty((cfg.layers, p0.num_slots, W.D_K), dtype=torch.bfloat16, device=dev)
+    qs = torch.empty((cfg.layers, p0.B * p0.T, p0.H, W.D_K), dtype=torch.bfloat16, device=dev)
+    for layer in range(cfg.layers):
+        m.fill_normal_bf16(pools[layer], W.tensor_seed(cfg.config_id, layer, W.STREAM_KV))
+        m.fill_normal_bf16(qs[layer], W.tensor_seed(cfg.config_id, layer, W.STREAM_Q))
+    desc = m.make_desc(p0.B, p0.T, p0.H, p0.num_slots, p0.stride, p0.max_seq_len, flags=m.DEFAULT_FLAGS)
+    ws = torch.empty(m.workspace_size(desc), dtype=torch.uint8, device=dev)
+    out = torch.empty((p0.B * p0.T, p0.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((p0.B * p0.T, p0.H), dtype=torch.float32, device=dev)
+    plan = m.plan(desc, torch.cuda.get_device_properties(dev).multi_processor_count)
+
+    def full_step(sp):
+        for layer in range(cfg.layers):
+            rc = m.verify_attn_raw(desc, qs[layer].data_ptr(), pools[layer].data_ptr(), st.data_ptr(), sl.data_ptr(),
+                                   tp.data_ptr(), out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), 0, sp)
+            if rc:
+                raise m.MLAError(rc, "mla_verify_attn")
+
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        full_step(stream.cuda_stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sp = torch.cuda.current_stream().cuda_stream
+        for _ in range(steps):
+            full_step(sp)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    step_s = e0.elapsed_time(e1) / 1e3 / steps
+    kv = W.kv_bytes_per_layer_step(p0.seq_lens, p0.T)
+    del g, pools, qs
+    torch.cuda.empty_cache()
+    return step_s, kv, plan, cfg.layers
+
+
 def run_gpu(args):
     import torch
     import speculative_decode_mla_gb300 as m
@@ -292,7 +342,27 @@ def run_gpu(args):
     c1.record(stream)
     torch.cuda.synchronize()
     combine_s = c0.elapsed_time(c1) / 1e3 / args.steps
-    attn_s = max(step_s - combine_s, 1e-9)
+
+    # the attention (split) kernel alone, through mla_verify_attn_partials, on the same rotated pools
+    def split_only(i, sptr):
+        r = i % L2_ROTATION
+        rc = m.verify_attn_partials_raw(desc, q.data_ptr(), pools[r].data_ptr(), tables[r].data_ptr(), sl.data_ptr(),
+                                        tp.data_ptr(), ws.data_ptr(), ws.numel(), 0, sptr)
+        if rc:
+            raise m.MLAError(rc, "mla_verify_attn_partials")
+
+    for i in range(3):
+        split_only(i, stream.cuda_stream)
+    agraph = capture(split_only, args.steps)
+    agraph.replay()
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    agraph.replay()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    attn_s = a0.elapsed_time(a1) / 1e3 / args.steps
+    del agraph, cgraph
 
     # end to end through the public call with host buffers
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
@@ -344,6 +414,18 @@ def run_gpu(args):
                 "sample": f"32 of {p.rows} query rows over the full visible set, extrapolated x{p.rows // 32}",
                 "us_per_layer_step": t_cpu * 1e6}
     clocks = clk.summary()
+    at_185k = None
+    if not args.no_185k:
+        s185, kv185, plan185, layers = measure_185k(m, W, dev, steps=max(3, min(args.steps, 10)), warmup=args.warmup)
+        s185 = max_over_ranks(s185, world)
+        gbs185 = sum_over_ranks(kv185, world) * layers / s185 / 1e9
+        at_185k = {"workload": ("185k full-depth step: 1 sequence, 184320-token prefix, random 32-node tree, "
+                                "8 heads, 61 layers each with its own 184352-slot pool (12.95 GB), shared slot table"),
+                   "us_per_layer_step": s185 / layers * 1e6, "ms_per_step": s185 * 1e3, "value": gbs185,
+                   "unit": "GB/s", "hbm_frac_of_8tbs": gbs185 / world / NOMINAL_HBM_GBS,
+                   "hbm_frac_of_measured": gbs185 / world / float(peaks()[0]["hbm_gbs"]),
+                   "splits": plan185.num_splits, "row_tiles": plan185.row_tiles,
+                   "steps": max(3, min(args.steps, 10)), "gpu_launches": 2 * layers * max(3, min(args.steps, 10))}
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -370,6 +452,8 @@ def run_gpu(args):
         }
         if base is not None:
             line["cpu_baseline"] = base
+        if at_185k is not None:
+            line["at_185k"] = at_185k
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -383,6 +467,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-185k", action="store_true", help="skip the 185k full-depth step measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

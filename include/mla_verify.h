@@ -155,6 +155,24 @@ int mla_verify_attn(const mla_verify_desc *desc, const void *q, const void *kv_p
                     int32_t *dev_status, mla_stream_t stream);
 
 /*
+ * mla_verify_attn_partials -- the split stage of mla_verify_attn alone: every
+ * (sequence, row tile, chunk) partial of the plan is written to `workspace`,
+ * and no combine is launched. With plan = mla_verify_plan(desc, SM count of the
+ * current device) and rows = B*T*H, the workspace then holds
+ *   part_o   float16 [plan.num_splits][rows][512] at workspace, and
+ *   part_lse float32 [plan.num_splits][rows] at the next 256-byte boundary after it,
+ * and mla_verify_combine(plan.num_splits, rows, 512, part_o, MLA_DTYPE_F16,
+ * part_lse, out, lse, desc->out_dtype, stream) then returns exactly what
+ * mla_verify_attn returns for the same inputs. Use it to time or schedule the two
+ * stages separately. Arguments, checks and return codes are those of
+ * mla_verify_attn without out and lse.
+ */
+int mla_verify_attn_partials(const mla_verify_desc *desc, const void *q, const void *kv_pool,
+                             const int32_t *slot_table, const int32_t *seq_lens, const int32_t *tree_parent,
+                             void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                             mla_stream_t stream);
+
+/*
  * mla_verify_combine -- LSE-weighted merge of split partials (flash-decoding
  * combine). For each row r:
  *   lse[r] = ln sum_s exp(part_lse[s][r]);  out[r] = sum_s exp(part_lse[s][r] - lse[r]) * part_o[s][r]

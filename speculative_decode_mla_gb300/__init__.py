@@ -64,12 +64,13 @@ def load_library(path: str = LIB_PATH):
     lib.mla_verify_plan.argtypes = [ctypes.POINTER(Desc), i32, ctypes.POINTER(Plan)]
     lib.mla_verify_workspace_size.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(ctypes.c_size_t)]
     lib.mla_verify_attn.argtypes = [ctypes.POINTER(Desc), P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
+    lib.mla_verify_attn_partials.argtypes = [ctypes.POINTER(Desc), P, P, P, P, P, P, ctypes.c_size_t, P, P]
     lib.mla_verify_combine.argtypes = [i32, i64, i32, P, i32, P, P, P, i32, P]
     lib.mla_verify_status_string.argtypes = [ctypes.c_int]
     lib.mla_verify_status_string.restype = ctypes.c_char_p
     lib.mla_fill_normal_bf16.argtypes = [P, i64, ctypes.c_uint64, ctypes.c_uint64, P]
-    for f in ("mla_verify_plan", "mla_verify_workspace_size", "mla_verify_attn", "mla_verify_combine",
-              "mla_fill_normal_bf16"):
+    for f in ("mla_verify_plan", "mla_verify_workspace_size", "mla_verify_attn", "mla_verify_attn_partials",
+              "mla_verify_combine", "mla_fill_normal_bf16"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -117,6 +118,23 @@ def verify_attn_raw(desc: Desc, q: int, kv_pool: int, slot_table: int, seq_lens:
     """Direct C-ABI call with integer device pointers; returns the status code."""
     return load_library().mla_verify_attn(ctypes.byref(desc), q, kv_pool, slot_table, seq_lens, tree_parent, out,
                                           lse, workspace, int(workspace_bytes), dev_status or None, stream or None)
+
+
+def verify_attn_partials_raw(desc: Desc, q: int, kv_pool: int, slot_table: int, seq_lens: int, tree_parent: int,
+                             workspace: int, workspace_bytes: int, dev_status: int, stream: int) -> int:
+    """Direct C-ABI call of the split stage alone (partials into the workspace); returns the status code."""
+    return load_library().mla_verify_attn_partials(ctypes.byref(desc), q, kv_pool, slot_table, seq_lens, tree_parent,
+                                                   workspace, int(workspace_bytes), dev_status or None, stream or None)
+
+
+def partials_views(workspace, plan: Plan, rows: int):
+    """(part_o fp16 [splits, rows, 512], part_lse fp32 [splits, rows]) views of a uint8 workspace tensor."""
+    import torch
+    o_bytes = plan.num_splits * rows * 512 * 2
+    l_off = (o_bytes + 255) // 256 * 256
+    part_o = workspace[:o_bytes].view(torch.float16).view(plan.num_splits, rows, 512)
+    part_l = workspace[l_off:l_off + plan.num_splits * rows * 4].view(torch.float32).view(plan.num_splits, rows)
+    return part_o, part_l
 
 
 def verify(q, kv_pool, slot_table, seq_lens, tree_parent, *, max_seq_len: int,

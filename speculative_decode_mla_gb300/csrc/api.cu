@@ -119,16 +119,17 @@ extern "C" int mla_verify_workspace_size(const mla_verify_desc* d, size_t* bytes
   return MLA_OK;
 }
 
-extern "C" int mla_verify_attn(const mla_verify_desc* d, const void* q, const void* kv_pool,
-                               const int32_t* slot_table, const int32_t* seq_lens, const int32_t* tree_parent,
-                               void* out, float* lse, void* workspace, size_t workspace_bytes,
-                               int32_t* dev_status, mla_stream_t stream) {
+namespace {
+// Checks, plans and launches the split (attention) kernel; *partials receive the workspace
+// layout. Shared by mla_verify_attn and mla_verify_attn_partials.
+int run_splits(const mla_verify_desc* d, const void* q, const void* kv_pool, const int32_t* slot_table,
+               const int32_t* seq_lens, const int32_t* tree_parent, void* workspace, size_t workspace_bytes,
+               int32_t* dev_status, cudaStream_t s, mla_verify_plan_t* plan_out, VerifyArgs* args_out) {
   int rc = check_desc(d);
   if (rc) return rc;
-  if (!q || !kv_pool || !slot_table || !seq_lens || !tree_parent || !out || !lse || !workspace)
-    return MLA_ERR_INVALID_ARGUMENT;
-  if (!aligned(q, 16) || !aligned(kv_pool, 16) || !aligned(out, 16) || !aligned(workspace, 256) ||
-      !aligned(lse, 4) || !aligned(slot_table, 4) || !aligned(seq_lens, 4) || !aligned(tree_parent, 4))
+  if (!q || !kv_pool || !slot_table || !seq_lens || !tree_parent || !workspace) return MLA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(kv_pool, 16) || !aligned(workspace, 256) || !aligned(slot_table, 4) ||
+      !aligned(seq_lens, 4) || !aligned(tree_parent, 4))
     return MLA_ERR_INVALID_ARGUMENT;
   const bool debug = (d->flags & MLA_FLAG_DEBUG_CHECKS) != 0;
   if (debug && !dev_status) return MLA_ERR_INVALID_ARGUMENT;
@@ -168,20 +169,55 @@ extern "C" int mla_verify_attn(const mla_verify_desc* d, const void* q, const vo
   a.scale = d->softmax_scale;
   a.scale_log2 = d->softmax_scale * 1.4426950408889634f;
 
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (debug && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess) return MLA_ERR_CUDA;
   cudaError_t e = p.kernel == 1 ? launch_verify_simt(a, s) : launch_verify_tc(a, s);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
-  e = launch_combine(p.num_splits, rows, kDLatent, a.part_o, MLA_DTYPE_F16, a.part_lse, out, lse, d->out_dtype,
-                     /*dependent=*/true, s);
-  if (e != cudaSuccess) return MLA_ERR_CUDA;
-  if (debug) {
-    int32_t h = 0;
-    if (cudaMemcpyAsync(&h, dev_status, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MLA_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
-    if (h != 0) return MLA_ERR_DEVICE_CHECK;
-  }
+  *plan_out = p;
+  *args_out = a;
   return MLA_OK;
+}
+
+// With debug checks: wait for the stream and turn a non-zero device status into an error.
+int finish_debug(const mla_verify_desc* d, int32_t* dev_status, cudaStream_t s) {
+  if (!(d->flags & MLA_FLAG_DEBUG_CHECKS)) return MLA_OK;
+  int32_t h = 0;
+  if (cudaMemcpyAsync(&h, dev_status, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
+  return h != 0 ? MLA_ERR_DEVICE_CHECK : MLA_OK;
+}
+}  // namespace
+
+extern "C" int mla_verify_attn(const mla_verify_desc* d, const void* q, const void* kv_pool,
+                               const int32_t* slot_table, const int32_t* seq_lens, const int32_t* tree_parent,
+                               void* out, float* lse, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_status, mla_stream_t stream) {
+  if (!out || !lse || !aligned(out, 16) || !aligned(lse, 4)) {
+    const int rc = check_desc(d);
+    return rc ? rc : MLA_ERR_INVALID_ARGUMENT;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mla_verify_plan_t p;
+  VerifyArgs a;
+  int rc = run_splits(d, q, kv_pool, slot_table, seq_lens, tree_parent, workspace, workspace_bytes, dev_status, s,
+                      &p, &a);
+  if (rc) return rc;
+  cudaError_t e = launch_combine(p.num_splits, a.rows, kDLatent, a.part_o, MLA_DTYPE_F16, a.part_lse, out, lse,
+                                 d->out_dtype, /*dependent=*/true, s);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  return finish_debug(d, dev_status, s);
+}
+
+extern "C" int mla_verify_attn_partials(const mla_verify_desc* d, const void* q, const void* kv_pool,
+                                        const int32_t* slot_table, const int32_t* seq_lens,
+                                        const int32_t* tree_parent, void* workspace, size_t workspace_bytes,
+                                        int32_t* dev_status, mla_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mla_verify_plan_t p;
+  VerifyArgs a;
+  int rc = run_splits(d, q, kv_pool, slot_table, seq_lens, tree_parent, workspace, workspace_bytes, dev_status, s,
+                      &p, &a);
+  if (rc) return rc;
+  return finish_debug(d, dev_status, s);
 }
 
 extern "C" int mla_verify_combine(int32_t num_splits, int64_t rows, int32_t d_v, const void* part_o,

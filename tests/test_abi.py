@@ -108,6 +108,17 @@ def test_attn_rejects_null_and_misaligned_pointers(lib):
     assert m.verify_attn_raw(dd, *args, 1 << 30, 0, 0) == -1  # debug checks need dev_status
 
 
+def test_partials_rejects_null_and_misaligned_pointers(lib):
+    d = desc()
+    fake = 1 << 20
+    f = m.verify_attn_partials_raw
+    assert f(d, 0, fake, fake, fake, fake, fake, 1 << 30, 0, 0) == -1         # null q
+    assert f(d, fake, fake, fake, fake, fake, 0, 1 << 30, 0, 0) == -1         # null workspace
+    assert f(d, fake, fake, fake, fake, fake, fake + 16, 1 << 30, 0, 0) == -1  # workspace not 256-B aligned
+    assert f(desc(flags=m.MLA_FLAG_DEBUG_CHECKS), fake, fake, fake, fake, fake, fake, 1 << 30, 0, 0) == -1
+    assert f(desc(num_nodes=0), fake, fake, fake, fake, fake, fake, 1 << 30, 0, 0) == -2
+
+
 def test_combine_rejects_bad_args(lib):
     f = lib.mla_verify_combine
     assert f(0, 4, 512, 16, 1, 16, 16, 16, 0, None) == -1      # no splits

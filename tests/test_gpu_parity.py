@@ -283,6 +283,34 @@ def test_combine_entry_point_matches_oracle_combine():
     assert_close(o.cpu().numpy().astype(np.float64), l.cpu().numpy(), full_o, full_l, "combine")
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_partials_then_combine_equals_attn(kernel):
+    """mla_verify_attn_partials + mla_verify_combine on its workspace is bit-identical to mla_verify_attn."""
+    import torch
+    import speculative_decode_mla_gb300 as m
+    p = W.custom_problem([5000, 130, 2047], 9, 13, seed=31, pool_slack=19)
+    q, kv, st, sl, tp = device_problem(p)
+    desc = m.make_desc(p.B, p.T, p.H, p.num_slots, p.stride, p.max_seq_len, flags=flags_of(kernel))
+    plan = m.plan(desc, torch.cuda.get_device_properties(0).multi_processor_count)
+    ws = torch.empty(m.workspace_size(desc), dtype=torch.uint8, device="cuda")
+    out = torch.empty((p.B * p.T, p.H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((p.B * p.T, p.H), dtype=torch.float32, device="cuda")
+    sp = torch.cuda.current_stream().cuda_stream
+    assert m.verify_attn_raw(desc, q.data_ptr(), kv.data_ptr(), st.data_ptr(), sl.data_ptr(), tp.data_ptr(),
+                             out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), 0, sp) == 0
+    ref_o, ref_l = out.clone(), lse.clone()
+    ws.fill_(0xAB)  # partials must be fully rewritten
+    assert m.verify_attn_partials_raw(desc, q.data_ptr(), kv.data_ptr(), st.data_ptr(), sl.data_ptr(),
+                                      tp.data_ptr(), ws.data_ptr(), ws.numel(), 0, sp) == 0
+    part_o, part_l = m.partials_views(ws, plan, p.rows)
+    o2, l2 = m.combine(part_o, part_l, out_dtype=m.MLA_DTYPE_BF16)
+    torch.cuda.synchronize()
+    assert torch.equal(o2.view(torch.int16), ref_o.view(p.rows, 512).view(torch.int16))
+    assert torch.equal(l2.view(-1), ref_l.view(-1))
+    ro, rl = oracle.verify_problem(p, SCALE)
+    assert_close(o2.float().cpu().numpy().astype(np.float64), l2.cpu().numpy().reshape(-1), ro, rl, "partials")
+
+
 # ------------------------------------------------------------------ input generator
 def test_device_generator_matches_host_bitwise():
     import torch

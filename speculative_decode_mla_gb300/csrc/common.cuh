@@ -1,6 +1,7 @@
 // Shared definitions of the tree-verify MLA attention library (host + device).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -45,6 +46,12 @@ cudaError_t launch_combine(int32_t splits, int64_t rows, int32_t d_v, const void
                            const float* part_lse, void* out, float* lse, int32_t out_dtype, bool dependent,
                            cudaStream_t stream);
 int tc_kernel_supported();
+// cuTensorMapEncodeTiled, looked up once through the runtime's driver entry point (no link to
+// libcuda); nullptr when the driver does not provide it.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
 
 // Device helpers ------------------------------------------------------------------------------
 __device__ __forceinline__ void report(int32_t* status, int debug, int bit) {

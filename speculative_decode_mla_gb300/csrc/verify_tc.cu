@@ -772,11 +772,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) TRACE(kTraceSlots - 2);
 }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no link to libcuda).
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-EncodeTiledFn encode_tiled() {
+}  // namespace
+
+EncodeTiledFn tensor_map_encoder() {
   static EncodeTiledFn fn = nullptr;
   if (fn == nullptr) {
     void* p = nullptr;
@@ -788,9 +786,7 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-}  // namespace
-
-int tc_kernel_supported() { return encode_tiled() != nullptr ? 1 : 0; }
+int tc_kernel_supported() { return tensor_map_encoder() != nullptr ? 1 : 0; }
 
 #ifdef MLA_TC_TRACE
 extern "C" int mla_tc_trace_set(void* buffer) {
@@ -818,7 +814,7 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream) {
   const cuuint64_t strides[2] = {(cuuint64_t)kDLatent * 2, (cuuint64_t)R * kDLatent * 2};
   const cuuint32_t box[3] = {64, (cuuint32_t)kRows, 1};
   const cuuint32_t elem[3] = {1, 1, 1};
-  EncodeTiledFn enc = encode_tiled();
+  EncodeTiledFn enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
   if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.part_o, dims, strides, box, elem,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,

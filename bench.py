@@ -237,6 +237,70 @@ def measure_185k(m, W, dev, steps, warmup):
     return step_s, kv, plan, cfg.layers
 
 
+def flush_l2(dev, buf=[]):
+    """Write a buffer larger than L2 so the next call starts with cold caches."""
+    import torch
+    if not buf:
+        buf.append(torch.empty(256 << 20, dtype=torch.uint8, device=dev))
+    buf[0].fill_(1)
+
+
+def measure_config(m, W, dev, name, steps):
+    """One named workload on a device-drawn pool: graph-replayed µs per call (back to back, same
+    pool) and the mean of 5 isolated calls, each after an L2 flush."""
+    import torch
+    p = W.make_problem(name, with_kv=False)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    pool = torch.empty((p.num_slots, W.D_K), dtype=torch.bfloat16, device=dev)
+    m.fill_normal_bf16(pool, p.kv_seed)
+    q = t(p.q.view(np.int16)).view(torch.bfloat16)
+    st, sl, tp = t(p.slot_table), t(p.seq_lens), t(p.tree_parent)
+    hint = int((p.seq_lens.astype(np.int64) + p.T).sum())
+    desc = m.make_desc(p.B, p.T, p.H, p.num_slots, p.stride, p.max_seq_len, flags=m.DEFAULT_FLAGS,
+                       total_tokens_hint=hint if p.B > 1 else 0)
+    ws = torch.empty(m.workspace_size(desc), dtype=torch.uint8, device=dev)
+    out = torch.empty((p.B * p.T, p.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((p.B * p.T, p.H), dtype=torch.float32, device=dev)
+    plan = m.plan(desc, torch.cuda.get_device_properties(dev).multi_processor_count)
+
+    def call(sp):
+        rc = m.verify_attn_raw(desc, q.data_ptr(), pool.data_ptr(), st.data_ptr(), sl.data_ptr(), tp.data_ptr(),
+                               out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), 0, sp)
+        if rc:
+            raise m.MLAError(rc, "mla_verify_attn")
+
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        call(stream.cuda_stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sp = torch.cuda.current_stream().cuda_stream
+        for _ in range(steps):
+            call(sp)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    graph_s = e0.elapsed_time(e1) / 1e3 / steps
+    iso = []
+    for _ in range(5):
+        flush_l2(dev)
+        e0.record(stream)
+        call(stream.cuda_stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        iso.append(e0.elapsed_time(e1) / 1e3)
+    kv = W.kv_bytes_per_layer_step(p.seq_lens, p.T)
+    del g, pool
+    torch.cuda.empty_cache()
+    return {"us_per_call": graph_s * 1e6, "isolated_us": float(np.mean(iso)) * 1e6,
+            "effective_kv_GBs": kv / graph_s / 1e9, "kv_bytes": kv, "splits": plan.num_splits,
+            "row_tiles": plan.row_tiles, "graph_steps": steps}
+
+
 def run_gpu(args):
     import torch
     import speculative_decode_mla_gb300 as m
@@ -414,6 +478,20 @@ def run_gpu(args):
                 "sample": f"32 of {p.rows} query rows over the full visible set, extrapolated x{p.rows // 32}",
                 "us_per_layer_step": t_cpu * 1e6}
     clocks = clk.summary()
+    # the metric's own config also as a single isolated call (L2 flushed before it)
+    iso = []
+    for _ in range(5):
+        flush_l2(dev)
+        e0.record(stream)
+        step(0, stream.cuda_stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        iso.append(e0.elapsed_time(e1) / 1e3)
+    isolated_s = float(np.mean(iso))
+    others = None
+    if not args.no_extra:
+        others = {name: measure_config(m, W, dev, name, steps=st_)
+                  for name, st_ in (("tiny", 50), ("batched", 20), ("wide", 5), ("wide_identity", 5))}
     at_185k = None
     if not args.no_185k:
         s185, kv185, plan185, layers = measure_185k(m, W, dev, steps=max(3, min(args.steps, 10)), warmup=args.warmup)
@@ -454,6 +532,9 @@ def run_gpu(args):
             line["cpu_baseline"] = base
         if at_185k is not None:
             line["at_185k"] = at_185k
+        line["isolated_us_per_layer_step"] = isolated_s * 1e6
+        if others is not None:
+            line["other_configs"] = others
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -468,6 +549,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-185k", action="store_true", help="skip the 185k full-depth step measurement")
+    ap.add_argument("--no-extra", action="store_true", help="skip the tiny/batched/wide timings")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -301,6 +301,55 @@ def measure_config(m, W, dev, name, steps):
             "row_tiles": plan.row_tiles, "graph_steps": steps}
 
 
+def measure_kv_ops(m, W, dev, p, pools, tables, steps):
+    """The KV-pool steps around verification on the 64k workload: Tier-0 compaction of the sequence's
+    65552 rows (read + write bytes, against the copy peak), tree-KV append and accept-commit (T = 16)."""
+    import torch
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    N = int(p.seq_lens[0]) + p.T
+    sl = t(p.seq_lens)
+    dst = torch.empty((N, W.D_K), dtype=torch.bfloat16, device=dev)
+    base = t(np.zeros(1, dtype=np.int64))
+    new_t = torch.empty_like(tables[0])
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for i in range(3):
+            fn(i)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(steps):
+                fn(i)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / steps
+
+    def compact(i):
+        r = i % len(pools)
+        m.kv_compact(pools[r], dst, tables[r], sl, base, num_nodes=p.T, max_seq_len=p.max_seq_len, new_slot_table=new_t)
+
+    s_compact = timed(compact)
+    moved = 2 * N * W.D_K * 2
+    tree_kv = torch.zeros((p.T, W.D_K), dtype=torch.bfloat16, device=dev)
+    pool_w = pools[0].clone()
+    s_append = timed(lambda i: m.tree_kv_append(pool_w, tree_kv, tables[0], sl, max_seq_len=p.max_seq_len))
+    st_w, sl_w, tp = tables[0].clone(), sl.clone(), t(p.tree_parent)
+    acc = t(np.full((1, p.T), -1, dtype=np.int32))
+    zero = t(np.zeros(1, dtype=np.int32))  # an empty accepted path: the call's cost without changing state
+    s_commit = timed(lambda i: m.tree_accept_commit(st_w, sl_w, tp, acc, zero, max_seq_len=p.max_seq_len))
+    peak = float(peaks()[0]["hbm_gbs"])
+    del pool_w, dst
+    return {"kv_compact": {"us": s_compact * 1e6, "rows": N, "read_plus_write_GBs": moved / s_compact / 1e9,
+                           "frac_of_measured_copy": moved / s_compact / 1e9 / peak},
+            "tree_kv_append_us": s_append * 1e6, "tree_accept_commit_us": s_commit * 1e6,
+            "tree_nodes": p.T}
+
+
 def run_gpu(args):
     import torch
     import speculative_decode_mla_gb300 as m
@@ -492,6 +541,7 @@ def run_gpu(args):
     if not args.no_extra:
         others = {name: measure_config(m, W, dev, name, steps=st_)
                   for name, st_ in (("tiny", 50), ("batched", 20), ("wide", 5), ("wide_identity", 5))}
+    kv_ops = None if args.no_extra else measure_kv_ops(m, W, dev, p, pools, tables, steps=20)
     at_185k = None
     if not args.no_185k:
         s185, kv185, plan185, layers = measure_185k(m, W, dev, steps=max(3, min(args.steps, 10)), warmup=args.warmup)
@@ -535,6 +585,8 @@ def run_gpu(args):
         line["isolated_us_per_layer_step"] = isolated_s * 1e6
         if others is not None:
             line["other_configs"] = others
+        if kv_ops is not None:
+            line["kv_pool_steps"] = kv_ops
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -178,3 +178,65 @@ def verify_problem(p, scale: float, rows=None, **kw):
     """``verify`` on a seeded problem object (fields seq_lens, slot_table, tree_parent, q, kv, H)."""
     return verify(p.seq_lens, p.slot_table, p.tree_parent, p.q, p.kv, num_heads=p.H, scale=scale,
                   rows=rows, **kw)
+
+
+# ---------------------------------------------------------------------------------------------
+# KV-pool steps around verification (plain numpy, the definitions written out). They follow
+# "The Moment of Certainty", The Final Piece (the tree nodes' rows live at their own slots,
+# and accepted nodes are scattered, so accepting a path rewrites the slot table) and "The Moment
+# of Reckoning (User Challenge...)", Output, item 4 (Tier-0 defragmentation keeps each request's
+# KV contiguous in the pool).
+
+def tree_kv_append(pool: np.ndarray, tree_kv: np.ndarray, slot_table: np.ndarray, seq_lens: np.ndarray,
+                   num_nodes: int) -> np.ndarray:
+    """pool[slot_table[b][L_b + j]] = tree_kv[b*T + j]; returns the new pool (the input is not modified)."""
+    out = pool.copy()
+    for b in range(len(seq_lens)):
+        L = int(seq_lens[b])
+        for j in range(num_nodes):
+            out[int(slot_table[b, L + j])] = tree_kv[b * num_nodes + j]
+    return out
+
+
+def tree_accept_commit(slot_table: np.ndarray, seq_lens: np.ndarray, tree_parent: np.ndarray,
+                       accepted: np.ndarray, num_accepted: np.ndarray, max_seq_len: int):
+    """Accepted path first (in path order) behind the prefix, then the rejected nodes in node order;
+    seq_lens += n. An invalid path (not root-first along parent links, n outside [0, T], or a prefix
+    longer than max_seq_len) leaves the sequence unchanged. Returns (table, lens, valid per sequence)."""
+    table = slot_table.copy()
+    lens = seq_lens.copy()
+    T = tree_parent.shape[1]
+    valid = np.zeros(len(seq_lens), dtype=bool)
+    for b in range(len(seq_lens)):
+        L, n = int(seq_lens[b]), int(num_accepted[b])
+        if not (0 <= L <= max_seq_len and 0 <= n <= T and L + n <= max_seq_len):
+            continue
+        path = [int(a) for a in accepted[b, :n]]
+        ok = all(0 <= a < T for a in path) and len(set(path)) == n
+        if ok:
+            for k, a in enumerate(path):
+                if int(tree_parent[b, a]) != (path[k - 1] if k else -1):
+                    ok = False
+        if not ok:
+            continue
+        old = [int(x) for x in slot_table[b, L:L + T]]
+        order = path + [j for j in range(T) if j not in path]
+        for pos, node in enumerate(order):
+            table[b, L + pos] = old[node]
+        lens[b] = L + n
+        valid[b] = True
+    return table, lens, valid
+
+
+def kv_compact(src_pool: np.ndarray, slot_table: np.ndarray, seq_lens: np.ndarray, num_nodes: int,
+               dst_base: np.ndarray, dst_slots: int):
+    """dst[dst_base[b] + t] = src[slot_table[b][t]] and new_table[b][t] = dst_base[b] + t for
+    t < L_b + T; rows of dst outside every range stay zero. Returns (dst, new_table)."""
+    dst = np.zeros((dst_slots,) + src_pool.shape[1:], dtype=src_pool.dtype)
+    table = slot_table.copy()
+    for b in range(len(seq_lens)):
+        for t in range(int(seq_lens[b]) + num_nodes):
+            d = int(dst_base[b]) + t
+            dst[d] = src_pool[int(slot_table[b, t])]
+            table[b, t] = d
+    return dst, table

@@ -69,8 +69,12 @@ def load_library(path: str = LIB_PATH):
     lib.mla_verify_status_string.argtypes = [ctypes.c_int]
     lib.mla_verify_status_string.restype = ctypes.c_char_p
     lib.mla_fill_normal_bf16.argtypes = [P, i64, ctypes.c_uint64, ctypes.c_uint64, P]
+    lib.mla_tree_kv_append.argtypes = [P, i64, P, P, P, i32, i32, i32, i32, i32, P, P]
+    lib.mla_tree_accept_commit.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, P, P]
+    lib.mla_kv_compact.argtypes = [P, i64, P, i64, P, P, P, P, i32, i32, i32, i32, i32, P, P]
     for f in ("mla_verify_plan", "mla_verify_workspace_size", "mla_verify_attn", "mla_verify_attn_partials",
-              "mla_verify_combine", "mla_fill_normal_bf16"):
+              "mla_verify_combine", "mla_fill_normal_bf16", "mla_tree_kv_append", "mla_tree_accept_commit",
+              "mla_kv_compact"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -187,6 +191,46 @@ def combine(part_o, part_lse, *, out_dtype: int = MLA_DTYPE_BF16, out=None, lse=
                                            out.data_ptr(), lse.data_ptr(), out_dtype, _stream_ptr(stream))
     _check(rc, "mla_verify_combine")
     return out, lse
+
+
+def tree_kv_append(pool, tree_kv, slot_table, seq_lens, *, max_seq_len: int, debug: bool = False,
+                   dev_status=None, stream=None):
+    """Write the tree nodes' rows into their slots (``include/mla_kv_ops.h``). pool bf16 [slots, 576],
+    tree_kv bf16 [B*T, 576], slot_table int32 [B, stride], seq_lens int32 [B]. In place on pool."""
+    B = seq_lens.shape[0]
+    T = tree_kv.shape[0] // B
+    rc = load_library().mla_tree_kv_append(pool.data_ptr(), pool.shape[0], tree_kv.data_ptr(), slot_table.data_ptr(),
+                                           seq_lens.data_ptr(), B, T, slot_table.shape[1], max_seq_len, int(debug),
+                                           _ptr_or_none(dev_status), _stream_ptr(stream))
+    _check(rc, "mla_tree_kv_append")
+    return pool
+
+
+def tree_accept_commit(slot_table, seq_lens, tree_parent, accepted, num_accepted, *, max_seq_len: int,
+                       debug: bool = False, dev_status=None, stream=None):
+    """Move the accepted path's slots behind the prefix and advance seq_lens (in place)."""
+    B, T = tree_parent.shape
+    rc = load_library().mla_tree_accept_commit(slot_table.data_ptr(), seq_lens.data_ptr(), tree_parent.data_ptr(),
+                                               accepted.data_ptr(), num_accepted.data_ptr(), B, T,
+                                               slot_table.shape[1], max_seq_len, int(debug),
+                                               _ptr_or_none(dev_status), _stream_ptr(stream))
+    _check(rc, "mla_tree_accept_commit")
+    return slot_table, seq_lens
+
+
+def kv_compact(src_pool, dst_pool, slot_table, seq_lens, dst_base, *, num_nodes: int, max_seq_len: int,
+               new_slot_table=None, debug: bool = False, dev_status=None, stream=None):
+    """Tier-0 compaction: copy each sequence's rows into dst_pool[dst_base[b]:] and rewrite new_slot_table."""
+    rc = load_library().mla_kv_compact(src_pool.data_ptr(), src_pool.shape[0], dst_pool.data_ptr(), dst_pool.shape[0],
+                                       slot_table.data_ptr(), _ptr_or_none(new_slot_table), seq_lens.data_ptr(),
+                                       dst_base.data_ptr(), seq_lens.shape[0], num_nodes, slot_table.shape[1],
+                                       max_seq_len, int(debug), _ptr_or_none(dev_status), _stream_ptr(stream))
+    _check(rc, "mla_kv_compact")
+    return dst_pool, new_slot_table
+
+
+def _ptr_or_none(t):
+    return None if t is None else t.data_ptr()
 
 
 def fill_normal_bf16(dst, seed: int, start: int = 0, stream=None):

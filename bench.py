@@ -344,10 +344,53 @@ def measure_kv_ops(m, W, dev, p, pools, tables, steps):
     s_commit = timed(lambda i: m.tree_accept_commit(st_w, sl_w, tp, acc, zero, max_seq_len=p.max_seq_len))
     peak = float(peaks()[0]["hbm_gbs"])
     del pool_w, dst
+
+    # Hybrid addressing on compacted pools: each rotated pool compacted to one contiguous prefix at
+    # slot 0 (tree after it), then the same verify through the slot table and through
+    # mla_verify_attn_hybrid (2-D TMA tiles for the prefix). 4 pools x 76 MB defeat L2.
+    L = int(p.seq_lens[0])
+    q = t(p.q.view(np.int16)).view(torch.bfloat16)
+    tp = t(p.tree_parent)
+    cpools, ctables = [], []
+    for r in range(len(pools)):
+        cp_ = torch.empty((N, W.D_K), dtype=torch.bfloat16, device=dev)
+        ct = torch.empty_like(tables[r])
+        m.kv_compact(pools[r], cp_, tables[r], sl, base, num_nodes=p.T, max_seq_len=p.max_seq_len, new_slot_table=ct)
+        cpools.append(cp_)
+        ctables.append(ct)
+    tree = ctables[0][:, L:L + p.T].contiguous()
+    zero64 = t(np.zeros(1, dtype=np.int64))
+    desc = m.make_desc(p.B, p.T, p.H, N, p.stride, p.max_seq_len, flags=m.DEFAULT_FLAGS)
+    ws = torch.empty(m.workspace_size(desc), dtype=torch.uint8, device=dev)
+    out = torch.empty((p.T, p.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((p.T, p.H), dtype=torch.float32, device=dev)
+    tp_ = t(p.tree_parent)
+
+    def via_table(i):
+        r = i % len(cpools)
+        rc = m.verify_attn_raw(desc, q.data_ptr(), cpools[r].data_ptr(), ctables[r].data_ptr(), sl.data_ptr(),
+                               tp_.data_ptr(), out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), 0,
+                               torch.cuda.current_stream().cuda_stream)
+        assert rc == 0, rc
+
+    def via_hybrid(i):
+        r = i % len(cpools)
+        rc = m.verify_attn_hybrid_raw(desc, q.data_ptr(), cpools[r].data_ptr(), zero64.data_ptr(), tree.data_ptr(),
+                                      sl.data_ptr(), tp_.data_ptr(), out.data_ptr(), lse.data_ptr(), ws.data_ptr(),
+                                      ws.numel(), 0, torch.cuda.current_stream().cuda_stream)
+        assert rc == 0, rc
+
+    s_table = timed(via_table)
+    s_hybrid = timed(via_hybrid)
+    del cpools, ctables
     return {"kv_compact": {"us": s_compact * 1e6, "rows": N, "read_plus_write_GBs": moved / s_compact / 1e9,
                            "frac_of_measured_copy": moved / s_compact / 1e9 / peak},
             "tree_kv_append_us": s_append * 1e6, "tree_accept_commit_us": s_commit * 1e6,
-            "tree_nodes": p.T}
+            "tree_nodes": p.T,
+            "hybrid_addressing_64k": {"workload": "64k verify on compacted pools (contiguous prefix, tree after it)",
+                                      "slot_table_us_per_layer_step": s_table * 1e6,
+                                      "hybrid_us_per_layer_step": s_hybrid * 1e6,
+                                      "hybrid_effective_kv_GBs": W.kv_bytes_per_layer_step(p.seq_lens, p.T) / s_hybrid / 1e9}}
 
 
 def run_gpu(args):

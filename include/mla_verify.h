@@ -173,6 +173,27 @@ int mla_verify_attn_partials(const mla_verify_desc *desc, const void *q, const v
                              mla_stream_t stream);
 
 /*
+ * mla_verify_attn_hybrid -- mla_verify_attn with hybrid addressing: each
+ * sequence's prefix is one contiguous range of the pool (base + length) and
+ * only the tree tail is addressed per token (page_size=1) -- the variant the
+ * pages propose ("Diagnosing Latency-Bound Decode", Broader Implications and
+ * Output; "The Moment of Certainty", The Path Forward), e.g. after
+ * mla_kv_compact has made the prefix contiguous.
+ *   prefix_base device int64 [B]: prefix position t < L_b is slot prefix_base[b] + t;
+ *               [prefix_base[b], prefix_base[b] + L_b) must lie in [0, num_slots).
+ *   tree_slots  device int32 [B][T]: tree node j of sequence b is slot tree_slots[b][j].
+ * There is no slot table: desc->slot_table_stride is ignored. Everything else
+ * (arguments, workspace, checks, return codes) is as for mla_verify_attn, and
+ * the result is bit-identical to mla_verify_attn over the slot table
+ * slot_table[b][t] = prefix_base[b] + t (t < L_b), tree_slots[b][t - L_b] (t >= L_b).
+ * Tiles of 64 positions wholly inside the prefix are loaded as 2-D TMA tiles.
+ */
+int mla_verify_attn_hybrid(const mla_verify_desc *desc, const void *q, const void *kv_pool,
+                           const int64_t *prefix_base, const int32_t *tree_slots, const int32_t *seq_lens,
+                           const int32_t *tree_parent, void *out, float *lse, void *workspace,
+                           size_t workspace_bytes, int32_t *dev_status, mla_stream_t stream);
+
+/*
  * mla_verify_combine -- LSE-weighted merge of split partials (flash-decoding
  * combine). For each row r:
  *   lse[r] = ln sum_s exp(part_lse[s][r]);  out[r] = sum_s exp(part_lse[s][r] - lse[r]) * part_o[s][r]

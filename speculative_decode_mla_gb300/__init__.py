@@ -65,6 +65,7 @@ def load_library(path: str = LIB_PATH):
     lib.mla_verify_workspace_size.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(ctypes.c_size_t)]
     lib.mla_verify_attn.argtypes = [ctypes.POINTER(Desc), P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
     lib.mla_verify_attn_partials.argtypes = [ctypes.POINTER(Desc), P, P, P, P, P, P, ctypes.c_size_t, P, P]
+    lib.mla_verify_attn_hybrid.argtypes = [ctypes.POINTER(Desc), P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
     lib.mla_verify_combine.argtypes = [i32, i64, i32, P, i32, P, P, P, i32, P]
     lib.mla_verify_status_string.argtypes = [ctypes.c_int]
     lib.mla_verify_status_string.restype = ctypes.c_char_p
@@ -73,6 +74,7 @@ def load_library(path: str = LIB_PATH):
     lib.mla_tree_accept_commit.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, P, P]
     lib.mla_kv_compact.argtypes = [P, i64, P, i64, P, P, P, P, i32, i32, i32, i32, i32, P, P]
     for f in ("mla_verify_plan", "mla_verify_workspace_size", "mla_verify_attn", "mla_verify_attn_partials",
+              "mla_verify_attn_hybrid",
               "mla_verify_combine", "mla_fill_normal_bf16", "mla_tree_kv_append", "mla_tree_accept_commit",
               "mla_kv_compact"):
         getattr(lib, f).restype = ctypes.c_int
@@ -122,6 +124,36 @@ def verify_attn_raw(desc: Desc, q: int, kv_pool: int, slot_table: int, seq_lens:
     """Direct C-ABI call with integer device pointers; returns the status code."""
     return load_library().mla_verify_attn(ctypes.byref(desc), q, kv_pool, slot_table, seq_lens, tree_parent, out,
                                           lse, workspace, int(workspace_bytes), dev_status or None, stream or None)
+
+
+def verify_attn_hybrid_raw(desc: Desc, q: int, kv_pool: int, prefix_base: int, tree_slots: int, seq_lens: int,
+                           tree_parent: int, out: int, lse: int, workspace: int, workspace_bytes: int, dev_status: int,
+                           stream: int) -> int:
+    """Direct C-ABI call of the hybrid-addressing verify (contiguous prefix + per-node tree slots)."""
+    return load_library().mla_verify_attn_hybrid(ctypes.byref(desc), q, kv_pool, prefix_base, tree_slots, seq_lens,
+                                                 tree_parent, out, lse, workspace, int(workspace_bytes),
+                                                 dev_status or None, stream or None)
+
+
+def verify_hybrid(q, kv_pool, prefix_base, tree_slots, seq_lens, tree_parent, *, max_seq_len: int,
+                  softmax_scale: float = DEFAULT_SCALE, out_dtype: int = MLA_DTYPE_BF16, flags: Optional[int] = None,
+                  num_splits: int = 0, dev_status=None, stream=None):
+    """Tree-verify attention with hybrid addressing: prefix position t of sequence b is slot
+    prefix_base[b] + t (int64 [B]); tree node j is slot tree_slots[b, j] (int32 [B, T])."""
+    import torch
+    B, T = tree_parent.shape
+    H = q.shape[1]
+    desc = make_desc(B, T, H, kv_pool.shape[0], max_seq_len + T, max_seq_len, softmax_scale=softmax_scale,
+                     out_dtype=out_dtype, flags=DEFAULT_FLAGS if flags is None else flags, num_splits=num_splits)
+    ws = torch.empty(workspace_size(desc), dtype=torch.uint8, device=q.device)
+    out = torch.empty((B * T, H, 512), device=q.device,
+                      dtype=torch.bfloat16 if out_dtype == MLA_DTYPE_BF16 else torch.float32)
+    lse = torch.empty((B * T, H), dtype=torch.float32, device=q.device)
+    rc = verify_attn_hybrid_raw(desc, q.data_ptr(), kv_pool.data_ptr(), prefix_base.data_ptr(), tree_slots.data_ptr(),
+                                seq_lens.data_ptr(), tree_parent.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                ws.data_ptr(), ws.numel(), _ptr_or_none(dev_status), _stream_ptr(stream))
+    _check(rc, "mla_verify_attn_hybrid")
+    return out, lse
 
 
 def verify_attn_partials_raw(desc: Desc, q: int, kv_pool: int, slot_table: int, seq_lens: int, tree_parent: int,

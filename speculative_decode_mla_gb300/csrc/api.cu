@@ -124,12 +124,17 @@ namespace {
 // layout. Shared by mla_verify_attn and mla_verify_attn_partials.
 int run_splits(const mla_verify_desc* d, const void* q, const void* kv_pool, const int32_t* slot_table,
                const int32_t* seq_lens, const int32_t* tree_parent, void* workspace, size_t workspace_bytes,
-               int32_t* dev_status, cudaStream_t s, mla_verify_plan_t* plan_out, VerifyArgs* args_out) {
+               int32_t* dev_status, cudaStream_t s, mla_verify_plan_t* plan_out, VerifyArgs* args_out,
+               const int64_t* prefix_base = nullptr, const int32_t* tree_slots = nullptr) {
+  const bool hybrid = prefix_base != nullptr;
   int rc = check_desc(d);
   if (rc) return rc;
-  if (!q || !kv_pool || !slot_table || !seq_lens || !tree_parent || !workspace) return MLA_ERR_INVALID_ARGUMENT;
-  if (!aligned(q, 16) || !aligned(kv_pool, 16) || !aligned(workspace, 256) || !aligned(slot_table, 4) ||
-      !aligned(seq_lens, 4) || !aligned(tree_parent, 4))
+  if (!q || !kv_pool || !seq_lens || !tree_parent || !workspace) return MLA_ERR_INVALID_ARGUMENT;
+  if (hybrid ? (!tree_slots || !aligned(prefix_base, 8) || !aligned(tree_slots, 4))
+             : (!slot_table || !aligned(slot_table, 4)))
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(kv_pool, 16) || !aligned(workspace, 256) || !aligned(seq_lens, 4) ||
+      !aligned(tree_parent, 4))
     return MLA_ERR_INVALID_ARGUMENT;
   const bool debug = (d->flags & MLA_FLAG_DEBUG_CHECKS) != 0;
   if (debug && !dev_status) return MLA_ERR_INVALID_ARGUMENT;
@@ -147,7 +152,10 @@ int run_splits(const mla_verify_desc* d, const void* q, const void* kv_pool, con
   memset(&a, 0, sizeof a);
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.kv = static_cast<const __nv_bfloat16*>(kv_pool);
-  a.slot_table = slot_table;
+  a.slot_table = hybrid ? nullptr : slot_table;
+  a.prefix_base = prefix_base;
+  a.tree_slots = tree_slots;
+  a.hybrid = hybrid ? 1 : 0;
   a.seq_lens = seq_lens;
   a.tree_parent = tree_parent;
   a.part_o = static_cast<__half*>(workspace);
@@ -217,6 +225,32 @@ extern "C" int mla_verify_attn_partials(const mla_verify_desc* d, const void* q,
   int rc = run_splits(d, q, kv_pool, slot_table, seq_lens, tree_parent, workspace, workspace_bytes, dev_status, s,
                       &p, &a);
   if (rc) return rc;
+  return finish_debug(d, dev_status, s);
+}
+
+extern "C" int mla_verify_attn_hybrid(const mla_verify_desc* d, const void* q, const void* kv_pool,
+                                      const int64_t* prefix_base, const int32_t* tree_slots, const int32_t* seq_lens,
+                                      const int32_t* tree_parent, void* out, float* lse, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, mla_stream_t stream) {
+  if (!d) return MLA_ERR_INVALID_ARGUMENT;
+  if (!prefix_base) return MLA_ERR_INVALID_ARGUMENT;
+  mla_verify_desc dh = *d;  // there is no slot table: its stride only has to pass the shared checks
+  dh.slot_table_stride = (int32_t)((int64_t)d->max_seq_len + d->num_nodes > 0x7fffffff
+                                       ? 0x7fffffff
+                                       : (int64_t)d->max_seq_len + d->num_nodes);
+  if (!out || !lse || !aligned(out, 16) || !aligned(lse, 4)) {
+    const int rc = check_desc(&dh);
+    return rc ? rc : MLA_ERR_INVALID_ARGUMENT;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mla_verify_plan_t p;
+  VerifyArgs a;
+  int rc = run_splits(&dh, q, kv_pool, nullptr, seq_lens, tree_parent, workspace, workspace_bytes, dev_status, s,
+                      &p, &a, prefix_base, tree_slots);
+  if (rc) return rc;
+  cudaError_t e = launch_combine(p.num_splits, a.rows, kDLatent, a.part_o, MLA_DTYPE_F16, a.part_lse, out, lse,
+                                 d->out_dtype, /*dependent=*/true, s);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
   return finish_debug(d, dev_status, s);
 }
 

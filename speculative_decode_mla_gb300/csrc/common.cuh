@@ -21,7 +21,9 @@ constexpr int kMaxNodes = 64;            // tree nodes per sequence (one u64 anc
 struct VerifyArgs {
   const __nv_bfloat16* q;
   const __nv_bfloat16* kv;
-  const int32_t* slot_table;
+  const int32_t* slot_table;    // [B][stride]; unused when hybrid
+  const int64_t* prefix_base;   // hybrid addressing: prefix position t of sequence b is slot prefix_base[b] + t
+  const int32_t* tree_slots;    // hybrid addressing: tree node j of sequence b is slot tree_slots[b*T + j]
   const int32_t* seq_lens;
   const int32_t* tree_parent;
   __half* part_o;     // [splits][rows][512] fp16, each split normalised over its own part
@@ -32,6 +34,7 @@ struct VerifyArgs {
   int32_t B, T, H, stride, max_seq_len;
   int32_t chunk, splits, row_tiles, rows_per_tile;
   int32_t debug;
+  int32_t hybrid;     // 1: prefix_base / tree_slots addressing, 0: slot_table
   float scale;        // softmax scale
   float scale_log2;   // softmax scale * log2(e)
 };
@@ -86,9 +89,16 @@ __device__ __forceinline__ uint64_t ancestor_mask(const VerifyArgs& a, int b, in
   return m;
 }
 
-// Physical slot of position t of sequence b, clamped into [0, num_slots).
-__device__ __forceinline__ int64_t load_slot(const VerifyArgs& a, int b, int64_t t) {
-  int64_t s = a.slot_table[(int64_t)b * a.stride + t];
+// Slot of logical position t of sequence b (prefix length L): the slot table's entry, or with
+// hybrid addressing the contiguous prefix base + t for t < L and the tree node's own slot after.
+__device__ __forceinline__ int64_t slot_of(const VerifyArgs& a, int b, int32_t L, int64_t t) {
+  if (!a.hybrid) return a.slot_table[(int64_t)b * a.stride + t];
+  return t < L ? a.prefix_base[b] + t : (int64_t)a.tree_slots[(int64_t)b * a.T + (t - L)];
+}
+
+// Physical slot of position t of sequence b (prefix length L), clamped into [0, num_slots).
+__device__ __forceinline__ int64_t load_slot(const VerifyArgs& a, int b, int32_t L, int64_t t) {
+  int64_t s = slot_of(a, b, L, t);
   if (s < 0 || s >= a.num_slots) {
     report(a.dev_status, a.debug, MLA_CHECK_BAD_SLOT);
     s = s < 0 ? 0 : a.num_slots - 1;

@@ -5,7 +5,8 @@
 //   grid.x = (sequence b, 8-row tile), grid.y = split index s; 8 warps per CTA.
 //   For each position t of the chunk [s*chunk, (s+1)*chunk) that row r can see
 //   (prefix t < L_b, or tree position L_b + j with j in anc*(i)), the warp
-//   gathers the 1152-byte latent row kv[slot_table[b][t]] (page_size=1),
+//   gathers the 1152-byte latent row kv[slot_table[b][t]] (page_size=1; or, with hybrid
+//   addressing, the contiguous prefix row kv[prefix_base[b] + t] / the tree node's own slot),
 //   computes s_t = scale * <q_r, k_t> with a shuffle reduction, and folds it into
 //   an online softmax (running max m, running sum l, o += p * v_t).
 //   The partial o/l and lse = m + ln l go to the workspace; the combine merges.
@@ -54,7 +55,7 @@ __global__ void __launch_bounds__(kWarps * 32) verify_simt_kernel(VerifyArgs a) 
 
   for (int64_t t = t0; t < t1; ++t) {
     if (t >= L && !((anc >> (t - L)) & 1ull)) continue;
-    const int64_t slot = load_slot(a, b, t);
+    const int64_t slot = load_slot(a, b, L, t);
     const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(a.kv + slot * kDK);
     float2 kf[kKeyPairsPerLane];
 #pragma unroll

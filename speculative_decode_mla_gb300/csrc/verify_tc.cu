@@ -39,6 +39,7 @@
 // writes NaN lse for its rows so the result is visibly invalid, and exits.
 #include <cuda.h>
 #include <cuda_fp16.h>
+#include <string.h>
 
 #include "common.cuh"
 
@@ -226,7 +227,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // ------------------------------------------------------------------ the kernel
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    verify_tc_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap tmap_o) {
+    verify_tc_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap tmap_o,
+                     const __grid_constant__ CUtensorMap tmap_kv, const __grid_constant__ CUtensorMap tmap_rope) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -258,10 +260,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // The reads the set-up waits on are issued together, before anything waits on one: the slots
   // of the first kStages tiles (producer warp), the prefix length and the tree parents. The query
   // rows are read after the set-up, so they do not delay it.
-  const int32_t* tab = a.slot_table + (int64_t)b * a.stride;
+  const int32_t* tab = a.hybrid ? nullptr : a.slot_table + (int64_t)b * a.stride;
   int32_t sr[kStages];  // producer warp p, lane l: slot of row 16p + (l & 15) of each of the next kStages tiles
   const bool producer = warp < kProducerWarps;
-  if (producer) {
+  if (producer && !a.hybrid) {  // (hybrid addressing computes them once the prefix length is known)
     const int64_t pre_end = min(t0 + (int64_t)a.chunk, (int64_t)a.stride);  // stays inside this row
 #pragma unroll
     for (int j = 0; j < kStages; ++j) {
@@ -386,11 +388,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // that lane's copies so far have landed.
     const char* kvb = reinterpret_cast<const char*>(a.kv);
     const int row_base = warp * 16;
+    // The slot of lane l's row (16p + (l & 15)) at position pos; positions past the end read row 0
+    // (they are masked later).
+    auto slot_at = [&](int64_t pos) -> int32_t { return pos < t1 ? (int32_t)slot_of(a, b, L, pos) : 0; };
+    int64_t pbase = 0;  // hybrid addressing: slot of prefix position 0
 #pragma unroll
-    for (int j = 0; j < kStages; ++j) {  // positions past the end read row 0 (masked later)
+    for (int j = 0; j < kStages; ++j) {
       const int64_t pos = t0 + (int64_t)j * kKeys + row_base + (lane & 15);
-      if (pos >= t1) sr[j] = 0;
+      if (a.hybrid) sr[j] = slot_at(pos);
+      else if (pos >= t1) sr[j] = 0;
     }
+    if (a.hybrid) {
+      pbase = a.prefix_base[b];
+      if (pbase < 0 || pbase + L > a.num_slots) {
+        report(a.dev_status, a.debug, MLA_CHECK_BAD_SLOT);
+        pbase = pbase < 0 ? 0 : a.num_slots - 1;  // in range; the TMA path is not used then
+      }
+    }
+    const bool prefix_tiles_by_tma = a.hybrid && pbase + L <= a.num_slots && pbase + L < 0x7fffffffll;
     bool ok = true;
     for (int tb = 0; tb < ntiles && ok; tb += kStages) {
 #pragma unroll
@@ -405,7 +420,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int32_t sl_own = sr[j];
         {  // the slot of this lane's row of tile t + kStages, needed once this stage comes round again
           const int64_t pn = t0 + (int64_t)(t + kStages) * kKeys + row_base + (lane & 15);
-          sr[j] = pn < t1 ? tab[pn] : 0;
+          sr[j] = a.hybrid ? slot_at(pn) : (pn < t1 ? tab[pn] : 0);
+        }
+        const int64_t p0 = t0 + (int64_t)t * kKeys;
+        if (prefix_tiles_by_tma && p0 + kKeys <= L) {
+          // Hybrid addressing, a tile wholly inside the contiguous prefix: rows pbase + p0 ... + 63
+          // by 2-D TMA boxes that land in the same swizzled layouts (4 value blocks of 64 columns,
+          // then this CTA's 32 RoPE columns). One lane arms the stage with the byte count; every
+          // other producer lane arrives plainly, so the stage completes when the bytes land.
+          if (warp == 0 && lane == 0) {
+            const uint32_t full = bar(kBarKvFull + j);
+            mbar_arrive_expect_tx(full, kStageBytes);
+            const int y = (int)(pbase + p0);
+#pragma unroll
+            for (int vb = 0; vb < 4; ++vb)
+              asm volatile(
+                  "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+                  "%3}], [%4];" ::"r"(sbase + vb * kBlockBytes),
+                  "l"(&tmap_kv), "r"((int)rank * 256 + vb * 64), "r"(y), "r"(full)
+                  : "memory");
+            asm volatile(
+                "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+                "%3}], [%4];" ::"r"(sbase + 4 * kBlockBytes),
+                "l"(&tmap_rope), "r"(kDLatent + (int)rank * 32), "r"(y), "r"(full)
+                : "memory");
+          } else {
+            mbar_arrive(bar(kBarKvFull + j));
+          }
+          if (warp == 0 && lane == 0 && t < 24) TRACE(14 + 10 * t);
+          continue;
         }
         if (sl_own < 0 || (int64_t)sl_own >= a.num_slots) {
           report(a.dev_status, a.debug, MLA_CHECK_BAD_SLOT);
@@ -820,7 +863,24 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream) {
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  verify_tc_kernel<<<dim3((unsigned)(units * 2)), kThreads, kSmemBytes, stream>>>(a, tmap);
+  // Hybrid addressing: the pool as a 2-D tensor [num_slots][576] bf16 for the contiguous-prefix
+  // tiles; boxes of 64 rows x 64 columns (128B swizzle) and 64 rows x 32 RoPE columns (64B swizzle).
+  CUtensorMap tmap_kv, tmap_rope;
+  memset(&tmap_kv, 0, sizeof tmap_kv);
+  memset(&tmap_rope, 0, sizeof tmap_rope);
+  if (a.hybrid) {
+    const cuuint64_t kdims[2] = {(cuuint64_t)kDK, (cuuint64_t)a.num_slots};
+    const cuuint64_t kstrides[1] = {(cuuint64_t)kDK * 2};
+    const cuuint32_t kbox[2] = {64, (cuuint32_t)kKeys}, rbox[2] = {32, (cuuint32_t)kKeys}, kelem[2] = {1, 1};
+    if (enc(&tmap_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(a.kv), kdims, kstrides, kbox,
+            kelem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        enc(&tmap_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(a.kv), kdims, kstrides, rbox,
+            kelem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  verify_tc_kernel<<<dim3((unsigned)(units * 2)), kThreads, kSmemBytes, stream>>>(a, tmap, tmap_kv, tmap_rope);
   return cudaGetLastError();
 }
 

@@ -119,6 +119,17 @@ def test_partials_rejects_null_and_misaligned_pointers(lib):
     assert f(desc(num_nodes=0), fake, fake, fake, fake, fake, fake, 1 << 30, 0, 0) == -2
 
 
+def test_hybrid_rejects_null_and_misaligned_pointers(lib):
+    d = desc(slot_table_stride=0)  # ignored by the hybrid call
+    fake = 1 << 20
+    f = m.verify_attn_hybrid_raw
+    assert f(d, fake, fake, 0, fake, fake, fake, fake, fake, fake, 1 << 30, 0, 0) == -1      # no prefix_base
+    assert f(d, fake, fake, fake, 0, fake, fake, fake, fake, fake, 1 << 30, 0, 0) == -1      # no tree_slots
+    assert f(d, fake, fake, fake + 4, fake, fake, fake, fake, fake, fake, 1 << 30, 0, 0) == -1  # base not 8-B aligned
+    assert f(d, fake, fake, fake, fake, fake, fake, 0, fake, fake, 1 << 30, 0, 0) == -1      # no out
+    assert f(desc(num_nodes=65), fake, fake, fake, fake, fake, fake, fake, fake, fake, 1 << 30, 0, 0) == -2
+
+
 def test_combine_rejects_bad_args(lib):
     f = lib.mla_verify_combine
     assert f(0, 4, 512, 16, 1, 16, 16, 16, 0, None) == -1      # no splits

@@ -106,6 +106,9 @@ __global__ void __launch_bounds__(kWarps * 32)
 combine_kernel(int32_t splits, int64_t rows, int32_t d_v, const PT* __restrict__ part_o,
                const float* __restrict__ part_lse, void* __restrict__ out, float* __restrict__ lse,
                int32_t out_dtype) {
+  // the next kernel in the stream (e.g. the next layer's attention) may be scheduled now; it waits
+  // for this grid to finish before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");  // no-op unless launched as a dependent
   const int64_t r = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -151,6 +154,9 @@ __global__ void __launch_bounds__(kWarps * 32)
 combine_tma_kernel(const __grid_constant__ CUtensorMap tm, int32_t splits, int32_t box_splits, int64_t rows,
                    int32_t d_v, const float* __restrict__ part_lse, void* __restrict__ out, float* __restrict__ lse,
                    int32_t out_dtype) {
+  // the next kernel in the stream (e.g. the next layer's attention) may be scheduled now; it waits
+  // for this grid to finish before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");  // no-op unless launched as a dependent
   extern __shared__ __align__(128) uint8_t sm[];      // [box_splits][kCols] fp16
   __shared__ __align__(8) uint64_t bar;

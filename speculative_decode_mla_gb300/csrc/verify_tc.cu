@@ -256,6 +256,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int R = a.T * a.H;
   const int row0 = tile_idx * kRows;
   const int64_t t0 = (int64_t)s * a.chunk;
+  // Launched as a programmatic dependent: everything above read no global memory; from here on
+  // the inputs may have been written by the kernel before this one in the stream.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // The reads the set-up waits on are issued together, before anything waits on one: the slots
   // of the first kStages tiles (producer warp), the prefix length and the tree parents. The query
@@ -880,8 +883,19 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  verify_tc_kernel<<<dim3((unsigned)(units * 2)), kThreads, kSmemBytes, stream>>>(a, tmap, tmap_kv, tmap_rope);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the CTAs may be scheduled while the previous kernel in the
+  // stream drains; they wait for its results (griddepcontrol.wait) before the first global read.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(units * 2));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, verify_tc_kernel, a, tmap, tmap_kv, tmap_rope);
 }
 
 }  // namespace mla

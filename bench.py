@@ -245,9 +245,10 @@ def flush_l2(dev, buf=[]):
     buf[0].fill_(1)
 
 
-def measure_config(m, W, dev, name, steps):
+def measure_config(m, W, dev, name, steps, ragged=False):
     """One named workload on a device-drawn pool: graph-replayed µs per call (back to back, same
-    pool) and the mean of 5 isolated calls, each after an L2 flush."""
+    pool) and the mean of 5 isolated calls, each after an L2 flush. With ragged=True every sequence
+    gets a seeded tree size in 1..T (mla_verify_attn_ragged)."""
     import torch
     p = W.make_problem(name, with_kv=False)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
@@ -263,9 +264,16 @@ def measure_config(m, W, dev, name, steps):
     lse = torch.empty((p.B * p.T, p.H), dtype=torch.float32, device=dev)
     plan = m.plan(desc, torch.cuda.get_device_properties(dev).multi_processor_count)
 
+    sizes = t(np.random.default_rng(5).integers(1, p.T + 1, size=p.B).astype(np.int32)) if ragged else None
+
     def call(sp):
-        rc = m.verify_attn_raw(desc, q.data_ptr(), pool.data_ptr(), st.data_ptr(), sl.data_ptr(), tp.data_ptr(),
-                               out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), 0, sp)
+        if ragged:
+            rc = m.verify_attn_ragged_raw(desc, q.data_ptr(), pool.data_ptr(), st.data_ptr(), sl.data_ptr(),
+                                          sizes.data_ptr(), tp.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                          ws.data_ptr(), ws.numel(), 0, sp)
+        else:
+            rc = m.verify_attn_raw(desc, q.data_ptr(), pool.data_ptr(), st.data_ptr(), sl.data_ptr(), tp.data_ptr(),
+                                   out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), 0, sp)
         if rc:
             raise m.MLAError(rc, "mla_verify_attn")
 
@@ -294,6 +302,8 @@ def measure_config(m, W, dev, name, steps):
         torch.cuda.synchronize()
         iso.append(e0.elapsed_time(e1) / 1e3)
     kv = W.kv_bytes_per_layer_step(p.seq_lens, p.T)
+    if ragged:
+        kv = sum(W.kv_bytes_per_layer_step(p.seq_lens[b:b + 1], int(n)) for b, n in enumerate(sizes.cpu().numpy()))
     del g, pool
     torch.cuda.empty_cache()
     return {"us_per_call": graph_s * 1e6, "isolated_us": float(np.mean(iso)) * 1e6,
@@ -584,6 +594,7 @@ def run_gpu(args):
     if not args.no_extra:
         others = {name: measure_config(m, W, dev, name, steps=st_)
                   for name, st_ in (("tiny", 50), ("batched", 20), ("wide", 5), ("wide_identity", 5))}
+        others["batched_ragged_trees"] = measure_config(m, W, dev, "batched", steps=20, ragged=True)
     kv_ops = None if args.no_extra else measure_kv_ops(m, W, dev, p, pools, tables, steps=20)
     at_185k = None
     if not args.no_185k:

@@ -194,6 +194,25 @@ int mla_verify_attn_hybrid(const mla_verify_desc *desc, const void *q, const voi
                            size_t workspace_bytes, int32_t *dev_status, mla_stream_t stream);
 
 /*
+ * mla_verify_attn_ragged -- mla_verify_attn for a batch whose trees differ in
+ * size (batched verify with a ragged T per sequence; the pages' drafter builds
+ * trees of varying size, "The Moment of Doubt", Input). desc->num_nodes is the
+ * largest tree, T_max, and every buffer keeps the mla_verify_attn layout for it;
+ * sequence b has T_b = tree_sizes[b] (1 <= T_b <= T_max) nodes:
+ *   tree_sizes  device int32 [B].
+ *   slot_table  row b holds the prefix, then the T_b tree nodes' slots at [L_b, L_b + T_b).
+ *   tree_parent row b: entries [0, T_b) as for mla_verify_attn; the rest are ignored.
+ *   q, out, lse rows of nodes j >= T_b are padding: q is not read, out is 0 and lse is -inf.
+ * A tree size outside [1, T_max] is clamped (MLA_CHECK_BAD_LENGTH under debug checks).
+ * Everything else is as for mla_verify_attn; with every T_b = T_max the result is
+ * bit-identical to it.
+ */
+int mla_verify_attn_ragged(const mla_verify_desc *desc, const void *q, const void *kv_pool,
+                           const int32_t *slot_table, const int32_t *seq_lens, const int32_t *tree_sizes,
+                           const int32_t *tree_parent, void *out, float *lse, void *workspace,
+                           size_t workspace_bytes, int32_t *dev_status, mla_stream_t stream);
+
+/*
  * mla_verify_combine -- LSE-weighted merge of split partials (flash-decoding
  * combine). For each row r:
  *   lse[r] = ln sum_s exp(part_lse[s][r]);  out[r] = sum_s exp(part_lse[s][r] - lse[r]) * part_o[s][r]

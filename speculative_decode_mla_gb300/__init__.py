@@ -66,6 +66,7 @@ def load_library(path: str = LIB_PATH):
     lib.mla_verify_attn.argtypes = [ctypes.POINTER(Desc), P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
     lib.mla_verify_attn_partials.argtypes = [ctypes.POINTER(Desc), P, P, P, P, P, P, ctypes.c_size_t, P, P]
     lib.mla_verify_attn_hybrid.argtypes = [ctypes.POINTER(Desc), P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
+    lib.mla_verify_attn_ragged.argtypes = [ctypes.POINTER(Desc), P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
     lib.mla_verify_combine.argtypes = [i32, i64, i32, P, i32, P, P, P, i32, P]
     lib.mla_verify_status_string.argtypes = [ctypes.c_int]
     lib.mla_verify_status_string.restype = ctypes.c_char_p
@@ -74,7 +75,7 @@ def load_library(path: str = LIB_PATH):
     lib.mla_tree_accept_commit.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, P, P]
     lib.mla_kv_compact.argtypes = [P, i64, P, i64, P, P, P, P, i32, i32, i32, i32, i32, P, P]
     for f in ("mla_verify_plan", "mla_verify_workspace_size", "mla_verify_attn", "mla_verify_attn_partials",
-              "mla_verify_attn_hybrid",
+              "mla_verify_attn_hybrid", "mla_verify_attn_ragged",
               "mla_verify_combine", "mla_fill_normal_bf16", "mla_tree_kv_append", "mla_tree_accept_commit",
               "mla_kv_compact"):
         getattr(lib, f).restype = ctypes.c_int
@@ -156,6 +157,15 @@ def verify_hybrid(q, kv_pool, prefix_base, tree_slots, seq_lens, tree_parent, *,
     return out, lse
 
 
+def verify_attn_ragged_raw(desc: Desc, q: int, kv_pool: int, slot_table: int, seq_lens: int, tree_sizes: int,
+                           tree_parent: int, out: int, lse: int, workspace: int, workspace_bytes: int, dev_status: int,
+                           stream: int) -> int:
+    """Direct C-ABI call of the ragged-tree verify (tree_sizes int32 [B], T_b <= desc.num_nodes)."""
+    return load_library().mla_verify_attn_ragged(ctypes.byref(desc), q, kv_pool, slot_table, seq_lens, tree_sizes,
+                                                 tree_parent, out, lse, workspace, int(workspace_bytes),
+                                                 dev_status or None, stream or None)
+
+
 def verify_attn_partials_raw(desc: Desc, q: int, kv_pool: int, slot_table: int, seq_lens: int, tree_parent: int,
                              workspace: int, workspace_bytes: int, dev_status: int, stream: int) -> int:
     """Direct C-ABI call of the split stage alone (partials into the workspace); returns the status code."""
@@ -176,12 +186,13 @@ def partials_views(workspace, plan: Plan, rows: int):
 def verify(q, kv_pool, slot_table, seq_lens, tree_parent, *, max_seq_len: int,
            softmax_scale: float = DEFAULT_SCALE, out_dtype: int = MLA_DTYPE_BF16, flags: Optional[int] = None,
            num_splits: int = 0, total_tokens_hint: int = 0, out=None, lse=None, workspace=None,
-           dev_status=None, stream=None):
+           dev_status=None, stream=None, tree_sizes=None):
     """Tree-verify attention on torch CUDA tensors (see ``include/mla_verify.h``).
 
     q: bf16 [B*T, H, 576]; kv_pool: bf16 [num_slots, 576]; slot_table: int32 [B, stride];
     seq_lens: int32 [B]; tree_parent: int32 [B, T]. Returns (out [B*T, H, 512], lse [B*T, H]).
     Buffers may be passed in to avoid allocation (out, lse, workspace as a uint8 tensor).
+    tree_sizes (int32 [B], each in 1..T) selects the ragged-tree call (mla_verify_attn_ragged).
     """
     import torch
     B, T = tree_parent.shape
@@ -199,6 +210,13 @@ def verify(q, kv_pool, slot_table, seq_lens, tree_parent, *, max_seq_len: int,
         lse = torch.empty((B * T, H), device=dev, dtype=torch.float32)
     if workspace is None:
         workspace = torch.empty(workspace_size(desc), device=dev, dtype=torch.uint8)
+    if tree_sizes is not None:
+        rc = verify_attn_ragged_raw(desc, q.data_ptr(), kv_pool.data_ptr(), slot_table.data_ptr(),
+                                    seq_lens.data_ptr(), tree_sizes.data_ptr(), tree_parent.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                    dev_status.data_ptr() if dev_status is not None else 0, _stream_ptr(stream))
+        _check(rc, "mla_verify_attn_ragged")
+        return out, lse
     rc = verify_attn_raw(desc, q.data_ptr(), kv_pool.data_ptr(), slot_table.data_ptr(), seq_lens.data_ptr(),
                          tree_parent.data_ptr(), out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
                          workspace.numel(), dev_status.data_ptr() if dev_status is not None else 0,

@@ -125,7 +125,8 @@ namespace {
 int run_splits(const mla_verify_desc* d, const void* q, const void* kv_pool, const int32_t* slot_table,
                const int32_t* seq_lens, const int32_t* tree_parent, void* workspace, size_t workspace_bytes,
                int32_t* dev_status, cudaStream_t s, mla_verify_plan_t* plan_out, VerifyArgs* args_out,
-               const int64_t* prefix_base = nullptr, const int32_t* tree_slots = nullptr) {
+               const int64_t* prefix_base = nullptr, const int32_t* tree_slots = nullptr,
+               const int32_t* tree_sizes = nullptr) {
   const bool hybrid = prefix_base != nullptr;
   int rc = check_desc(d);
   if (rc) return rc;
@@ -134,7 +135,7 @@ int run_splits(const mla_verify_desc* d, const void* q, const void* kv_pool, con
              : (!slot_table || !aligned(slot_table, 4)))
     return MLA_ERR_INVALID_ARGUMENT;
   if (!aligned(q, 16) || !aligned(kv_pool, 16) || !aligned(workspace, 256) || !aligned(seq_lens, 4) ||
-      !aligned(tree_parent, 4))
+      !aligned(tree_parent, 4) || !aligned(tree_sizes, 4))
     return MLA_ERR_INVALID_ARGUMENT;
   const bool debug = (d->flags & MLA_FLAG_DEBUG_CHECKS) != 0;
   if (debug && !dev_status) return MLA_ERR_INVALID_ARGUMENT;
@@ -155,6 +156,7 @@ int run_splits(const mla_verify_desc* d, const void* q, const void* kv_pool, con
   a.slot_table = hybrid ? nullptr : slot_table;
   a.prefix_base = prefix_base;
   a.tree_slots = tree_slots;
+  a.tree_sizes = tree_sizes;
   a.hybrid = hybrid ? 1 : 0;
   a.seq_lens = seq_lens;
   a.tree_parent = tree_parent;
@@ -247,6 +249,30 @@ extern "C" int mla_verify_attn_hybrid(const mla_verify_desc* d, const void* q, c
   VerifyArgs a;
   int rc = run_splits(&dh, q, kv_pool, nullptr, seq_lens, tree_parent, workspace, workspace_bytes, dev_status, s,
                       &p, &a, prefix_base, tree_slots);
+  if (rc) return rc;
+  cudaError_t e = launch_combine(p.num_splits, a.rows, kDLatent, a.part_o, MLA_DTYPE_F16, a.part_lse, out, lse,
+                                 d->out_dtype, /*dependent=*/true, s);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  return finish_debug(d, dev_status, s);
+}
+
+extern "C" int mla_verify_attn_ragged(const mla_verify_desc* d, const void* q, const void* kv_pool,
+                                      const int32_t* slot_table, const int32_t* seq_lens, const int32_t* tree_sizes,
+                                      const int32_t* tree_parent, void* out, float* lse, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, mla_stream_t stream) {
+  if (!tree_sizes) {
+    const int rc = check_desc(d);
+    return rc ? rc : MLA_ERR_INVALID_ARGUMENT;
+  }
+  if (!out || !lse || !aligned(out, 16) || !aligned(lse, 4)) {
+    const int rc = check_desc(d);
+    return rc ? rc : MLA_ERR_INVALID_ARGUMENT;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mla_verify_plan_t p;
+  VerifyArgs a;
+  int rc = run_splits(d, q, kv_pool, slot_table, seq_lens, tree_parent, workspace, workspace_bytes, dev_status, s,
+                      &p, &a, nullptr, nullptr, tree_sizes);
   if (rc) return rc;
   cudaError_t e = launch_combine(p.num_splits, a.rows, kDLatent, a.part_o, MLA_DTYPE_F16, a.part_lse, out, lse,
                                  d->out_dtype, /*dependent=*/true, s);

@@ -24,6 +24,7 @@ struct VerifyArgs {
   const int32_t* slot_table;    // [B][stride]; unused when hybrid
   const int64_t* prefix_base;   // hybrid addressing: prefix position t of sequence b is slot prefix_base[b] + t
   const int32_t* tree_slots;    // hybrid addressing: tree node j of sequence b is slot tree_slots[b*T + j]
+  const int32_t* tree_sizes;    // ragged trees: sequence b has tree_sizes[b] nodes (1..T); nullptr = T each
   const int32_t* seq_lens;
   const int32_t* tree_parent;
   __half* part_o;     // [splits][rows][512] fp16, each split normalised over its own part
@@ -69,6 +70,17 @@ __device__ __forceinline__ int32_t load_len(const VerifyArgs& a, int b) {
     L = L < 0 ? 0 : a.max_seq_len;
   }
   return L;
+}
+
+// Number of tree nodes of sequence b (T unless trees are ragged), clamped into [1, T].
+__device__ __forceinline__ int32_t load_tree_size(const VerifyArgs& a, int b) {
+  if (!a.tree_sizes) return a.T;
+  int32_t n = a.tree_sizes[b];
+  if (n < 1 || n > a.T) {
+    report(a.dev_status, a.debug, MLA_CHECK_BAD_LENGTH);
+    n = n < 1 ? 1 : a.T;
+  }
+  return n;
 }
 
 // Ancestor-or-self bit set of node i (bit j set iff j == i or j is an ancestor of i).

@@ -33,11 +33,12 @@ __global__ void __launch_bounds__(kWarps * 32) verify_simt_kernel(VerifyArgs a) 
   const int64_t row = (int64_t)b * R + local_row;
 
   const int32_t L = load_len(a, b);
-  const int64_t N = (int64_t)L + a.T;
+  const int32_t Tb = load_tree_size(a, b);
+  const int64_t N = (int64_t)L + Tb;
   const int64_t t0 = (int64_t)s * a.chunk;
   const int64_t t1 = min(N, t0 + a.chunk);
   __half* po = a.part_o + ((int64_t)s * a.rows + row) * kDLatent;
-  if (t0 >= t1) {
+  if (t0 >= t1 || i >= Tb) {  // nothing in this chunk, or a padding row of a smaller tree
     if (lane == 0) a.part_lse[(int64_t)s * a.rows + row] = -INFINITY;
     return;
   }

@@ -276,13 +276,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   const int32_t L_raw = a.seq_lens[b];
   const int32_t par_raw = threadIdx.x < a.T ? a.tree_parent[(int64_t)b * a.T + threadIdx.x] : -1;
+  const int32_t Tb = load_tree_size(a, b);  // this sequence's tree (T unless trees are ragged)
 
   int32_t L = L_raw;
   if (L < 0 || L > a.max_seq_len) {
     report(a.dev_status, a.debug, MLA_CHECK_BAD_LENGTH);
     L = L < 0 ? 0 : a.max_seq_len;
   }
-  const int64_t N = (int64_t)L + a.T;
+  const int64_t N = (int64_t)L + Tb;
   const int64_t t1 = min(N, t0 + a.chunk);
   if (t0 >= t1) {  // nothing of this sequence falls in this chunk: an empty partial (both CTAs agree)
     if (rank == 0 && threadIdx.x < kRows && row0 + (int)threadIdx.x < R)
@@ -316,7 +317,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x < a.T) {  // tree parents of this sequence, validated, into shared memory
     int p = par_raw;
-    if (p < -1 || p >= (int)threadIdx.x) {
+    if ((int)threadIdx.x >= Tb) {
+      p = -1;  // a padding node of a smaller tree
+    } else if (p < -1 || p >= (int)threadIdx.x) {
       report(a.dev_status, a.debug, MLA_CHECK_BAD_PARENT);
       p = -1;
     }
@@ -352,7 +355,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const bool q_sender = warp >= kSenderWarp0;
     const int q_row = (warp & 3) * 32 + lane;  // tile row = TMEM lane of this thread
     const int q_c0 = q_sender ? 20 : 0, q_n = q_sender ? 16 : 20;
-    const bool qvalid = row0 + q_row < R;
+    const bool qvalid = row0 + q_row < R && (row0 + q_row) / a.H < Tb;
     const uint4* qrow = reinterpret_cast<const uint4*>(a.q + (qvalid ? (int64_t)b * R + row0 + q_row : 0) * kDK);
     uint32_t qv[80];
 #pragma unroll
@@ -565,7 +568,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
     const int local_row = row0 + r;
     uint64_t anc = ~0ull;  // anc*(node): the tree positions this row can see
-    if (local_row < R) {
+    if (local_row < R && local_row / a.H < Tb) {
       anc = 0;
       for (int j = local_row / a.H, step = 0; j >= 0 && step < kMaxNodes; j = s_parent[j], ++step) anc |= 1ull << j;
     }
@@ -629,7 +632,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int r = q4 * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
     const int local_row = row0 + r;
-    const bool valid = local_row < R;
+    const bool valid = local_row < R && local_row / a.H < Tb;  // not past R, not a padding node
     const int64_t grow = (int64_t)b * R + local_row;
     const int node = valid ? local_row / a.H : 0;
 
@@ -795,9 +798,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
-      if (valid && rank == 0)
+      if (local_row < R && rank == 0)  // padding rows of a smaller tree carry no weight
         a.part_lse[(int64_t)s * a.rows + grow] =
-            l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+            (valid && l_run > 0.f) ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
       if (warp == kSoftmaxWarp0 && lane == 0) TRACE(kTraceSlots - 3);
     }
   }

@@ -130,6 +130,15 @@ def test_hybrid_rejects_null_and_misaligned_pointers(lib):
     assert f(desc(num_nodes=65), fake, fake, fake, fake, fake, fake, fake, fake, fake, 1 << 30, 0, 0) == -2
 
 
+def test_ragged_rejects_null_and_misaligned_tree_sizes(lib):
+    d = desc()
+    fake = 1 << 20
+    f = m.verify_attn_ragged_raw
+    assert f(d, fake, fake, fake, fake, 0, fake, fake, fake, fake, 1 << 30, 0, 0) == -1      # no tree_sizes
+    assert f(d, fake, fake, fake, fake, fake + 2, fake, fake, fake, fake, 1 << 30, 0, 0) == -1  # misaligned
+    assert f(desc(num_nodes=65), fake, fake, fake, fake, fake, fake, fake, fake, fake, 1 << 30, 0, 0) == -2
+
+
 def test_combine_rejects_bad_args(lib):
     f = lib.mla_verify_combine
     assert f(0, 4, 512, 16, 1, 16, 16, 16, 0, None) == -1      # no splits

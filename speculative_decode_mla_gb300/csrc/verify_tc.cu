@@ -76,8 +76,7 @@ constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;  // O 256, 
 constexpr int kBarKvFull = 0, kBarKvEmpty = kStages, kBarQFull = 2 * kStages, kBarSFull = kBarQFull + 1,
               kBarSEmpty = kBarQFull + 2, kBarPFull = kBarQFull + 3, kBarPEmpty = kBarQFull + 4,
               kBarXFull = kBarQFull + 5 /*2*/, kBarXEmpty = kBarQFull + 7 /*2*/, kBarXRead = kBarQFull + 9 /*2*/,
-              kBarDrainS = kBarQFull + 11, kBarDrainP = kBarQFull + 12, kBarEpi = kBarQFull + 13,
-              kNumBars = kBarQFull + 14;
+              kBarDrainS = kBarQFull + 11, kBarDrainP = kBarQFull + 12, kNumBars = kBarQFull + 13;
 static_assert(8 * kNumBars + 8 + 4 * kMaxNodes <= 512, "barrier area");
 
 constexpr long long kTimeoutCycles = 4000000000ll;  // ~2 s at 2 GHz
@@ -309,7 +308,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarPEmpty), 1);
     mbar_init(bar(kBarDrainS), 1);
     mbar_init(bar(kBarDrainP), 1);
-    mbar_init(bar(kBarEpi), 4);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     mbar_arrive_expect_tx(bar(kBarXFull + 0), kXBytes);  // first use of each exchange buffer
@@ -760,6 +758,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const int z = s * a.B + b;
+      // Each warp owns its 32 rows (its TMEM lane quarter) of every box and stores them itself, so
+      // the TMA store of box c overlaps the TMEM reads and conversion of box c + 1.
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {  // box c holds columns [64c, 64c + 64) of this CTA's half, fp16
         uint32_t o[64];
@@ -778,26 +779,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           box[u ^ (r & 7)] = make_uint4(w[0], w[1], w[2], w[3]);
         }
-      }
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarEpi));
-      if (warp == kSoftmaxWarp0) {
-        ok = wait_warp(bar(kBarEpi), 0, abort_flag);
-        if (ok && lane == 0) {
-          const int z = s * a.B + b;
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            asm volatile(
-                "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(&tmap_o),
-                "r"((int)rank * 256 + c * 64), "r"(row0), "r"(z), "r"(base + c * kEpiBoxBytes)
-                : "memory");
-          }
-          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-          asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-        }
+        fence_proxy_async();
         __syncwarp();
+        if (lane == 0) {
+          asm volatile(
+              "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(&tmap_o),
+              "r"((int)rank * 256 + c * 64), "r"(row0 + q4 * 32), "r"(z),
+              "r"(base + c * kEpiBoxBytes + q4 * 32 * 128)
+              : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
       }
+      if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      __syncwarp();
       if (local_row < R && rank == 0)  // padding rows of a smaller tree carry no weight
         a.part_lse[(int64_t)s * a.rows + grow] =
             (valid && l_run > 0.f) ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
@@ -855,13 +849,14 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream) {
   }
   const int64_t units = (int64_t)a.B * a.row_tiles * a.splits;
   if (units * 2 > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  // The split partials viewed as [splits * B][R][512] fp16; a store box is 64 columns x 128 rows,
-  // so rows past a sequence's R rows fall outside dimension 1 and are not written.
+  // The split partials viewed as [splits * B][R][512] fp16; a store box is 64 columns x 32 rows
+  // (one softmax warp's rows), so rows past a sequence's R rows fall outside dimension 1 and are
+  // not written.
   const int R = a.T * a.H;
   CUtensorMap tmap;
   const cuuint64_t dims[3] = {(cuuint64_t)kDLatent, (cuuint64_t)R, (cuuint64_t)a.splits * (cuuint64_t)a.B};
   const cuuint64_t strides[2] = {(cuuint64_t)kDLatent * 2, (cuuint64_t)R * kDLatent * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)kRows, 1};
+  const cuuint32_t box[3] = {64, 32, 1};
   const cuuint32_t elem[3] = {1, 1, 1};
   EncodeTiledFn enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;

@@ -69,7 +69,17 @@ enum mla_flags {
   MLA_FLAG_DEBUG_CHECKS = 1 << 0,
   /* Run the plain SIMT reference kernel (fp32 FMA, no tensor cores) instead of
    * the tcgen05 kernel. Same partial layout and combine; for tests and debugging. */
-  MLA_FLAG_SIMT = 1 << 1
+  MLA_FLAG_SIMT = 1 << 1,
+  /* A promise from the caller: the kernel enqueued just before this call on the
+   * stream does not write seq_lens, the prefix part of the slot table (entries
+   * [0, L_b)), prefix_base, or the prefix rows of kv_pool. The tcgen05 kernel is
+   * launched as a programmatic dependent of that kernel; with this flag its
+   * gather starts on the first prefix tiles before that kernel has finished
+   * (everything else -- q, the tree, tree sizes and slots -- is still read only
+   * after it). Typical use: consecutive layers of one decode step, whose
+   * prefixes were written by earlier steps. Results are identical with or
+   * without the flag when the promise holds. */
+  MLA_FLAG_PREFIX_STABLE = 1 << 2
 };
 
 /* Bits the device checks may set in *dev_status. */

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libmla_verify.so")
 
 MLA_OK = 0
 MLA_DTYPE_BF16, MLA_DTYPE_F32, MLA_DTYPE_F16 = 0, 1, 2
-MLA_FLAG_DEBUG_CHECKS, MLA_FLAG_SIMT = 1, 2
+MLA_FLAG_DEBUG_CHECKS, MLA_FLAG_SIMT, MLA_FLAG_PREFIX_STABLE = 1, 2, 4
 CHECK_BAD_SLOT, CHECK_BAD_PARENT, CHECK_BAD_LENGTH, CHECK_TIMEOUT = 1, 2, 4, 8
 D_LATENT, D_ROPE = 512, 64
 DEFAULT_SCALE = 1.0 / math.sqrt(192.0)

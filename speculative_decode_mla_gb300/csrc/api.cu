@@ -26,7 +26,7 @@ int check_desc(const mla_verify_desc* d) {
   if ((int64_t)d->slot_table_stride < (int64_t)d->max_seq_len + d->num_nodes) return MLA_ERR_INVALID_ARGUMENT;
   if (!isfinite(d->softmax_scale) || !(d->softmax_scale > 0.f)) return MLA_ERR_INVALID_ARGUMENT;
   if (d->out_dtype != MLA_DTYPE_BF16 && d->out_dtype != MLA_DTYPE_F32) return MLA_ERR_INVALID_ARGUMENT;
-  if (d->flags & ~(MLA_FLAG_DEBUG_CHECKS | MLA_FLAG_SIMT)) return MLA_ERR_INVALID_ARGUMENT;
+  if (d->flags & ~(MLA_FLAG_DEBUG_CHECKS | MLA_FLAG_SIMT | MLA_FLAG_PREFIX_STABLE)) return MLA_ERR_INVALID_ARGUMENT;
   if (d->num_splits < 0 || d->num_splits > kMaxSplits || d->total_tokens_hint < 0) return MLA_ERR_INVALID_ARGUMENT;
   const int64_t rows = (int64_t)d->num_seqs * d->num_nodes * d->num_heads;
   if (rows > (1ll << 31) - 1) return MLA_ERR_UNSUPPORTED;
@@ -158,6 +158,7 @@ int run_splits(const mla_verify_desc* d, const void* q, const void* kv_pool, con
   a.tree_slots = tree_slots;
   a.tree_sizes = tree_sizes;
   a.hybrid = hybrid ? 1 : 0;
+  a.early_prefix = (d->flags & MLA_FLAG_PREFIX_STABLE) ? 1 : 0;
   a.seq_lens = seq_lens;
   a.tree_parent = tree_parent;
   a.part_o = static_cast<__half*>(workspace);

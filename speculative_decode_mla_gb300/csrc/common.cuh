@@ -36,6 +36,7 @@ struct VerifyArgs {
   int32_t chunk, splits, row_tiles, rows_per_tile;
   int32_t debug;
   int32_t hybrid;     // 1: prefix_base / tree_slots addressing, 0: slot_table
+  int32_t early_prefix;  // MLA_FLAG_PREFIX_STABLE: the prefix may be gathered before the preceding kernel ends
   float scale;        // softmax scale
   float scale_log2;   // softmax scale * log2(e)
 };

@@ -68,6 +68,7 @@ constexpr int kReleaseWarp = 6;     // tells the partner when a receive buffer h
 constexpr int kSoftmaxWarp0 = 7;    // warps 7..10: TMEM lane quarters 3, 0, 1, 2
 constexpr int kSenderWarp0 = 11;    // warps 11..14: TMEM lane quarters 3, 0, 1, 2
 constexpr int kThreads = 15 * 32;
+constexpr int kParentThread0 = kSIssueWarp * 32;  // threads reading the tree parents (T <= 64: warps 4-5)
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;  // O 256, S 64, P 32, Q 144 columns
@@ -256,15 +257,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int row0 = tile_idx * kRows;
   const int64_t t0 = (int64_t)s * a.chunk;
   // Launched as a programmatic dependent: everything above read no global memory; from here on
-  // the inputs may have been written by the kernel before this one in the stream.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the inputs may have been written by the kernel before this one in the stream. With
+  // MLA_FLAG_PREFIX_STABLE the producer warps may read the prefix (length, slots, rows) first and
+  // wait just before anything else (see the producer section).
+  const bool producer = warp < kProducerWarps;
+  const bool early_ok = a.early_prefix && producer;
+  if (!early_ok) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // The reads the set-up waits on are issued together, before anything waits on one: the slots
   // of the first kStages tiles (producer warp), the prefix length and the tree parents. The query
   // rows are read after the set-up, so they do not delay it.
   const int32_t* tab = a.hybrid ? nullptr : a.slot_table + (int64_t)b * a.stride;
   int32_t sr[kStages];  // producer warp p, lane l: slot of row 16p + (l & 15) of each of the next kStages tiles
-  const bool producer = warp < kProducerWarps;
   if (producer && !a.hybrid) {  // (hybrid addressing computes them once the prefix length is known)
     const int64_t pre_end = min(t0 + (int64_t)a.chunk, (int64_t)a.stride);  // stays inside this row
 #pragma unroll
@@ -274,22 +278,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   }
   const int32_t L_raw = a.seq_lens[b];
-  const int32_t par_raw = threadIdx.x < a.T ? a.tree_parent[(int64_t)b * a.T + threadIdx.x] : -1;
-  const int32_t Tb = load_tree_size(a, b);  // this sequence's tree (T unless trees are ragged)
+  // the tree parents are read by warps 4-5 (never early), and T <= 64
+  const int pidx = (int)threadIdx.x - kParentThread0;
+  const int32_t par_raw = (pidx >= 0 && pidx < a.T) ? a.tree_parent[(int64_t)b * a.T + pidx] : -1;
 
   int32_t L = L_raw;
   if (L < 0 || L > a.max_seq_len) {
     report(a.dev_status, a.debug, MLA_CHECK_BAD_LENGTH);
     L = L < 0 ? 0 : a.max_seq_len;
   }
-  const int64_t N = (int64_t)L + Tb;
-  const int64_t t1 = min(N, t0 + a.chunk);
-  if (t0 >= t1) {  // nothing of this sequence falls in this chunk: an empty partial (both CTAs agree)
+  // Early prefix tiles: the chunk's first (up to kStages) tiles that lie wholly inside the prefix.
+  // A producer warp with some issues them before waiting; otherwise it waits here.
+  int early_tiles = 0;
+  if (early_ok) {
+    if (t0 < L) early_tiles = (int)min((int64_t)kStages, (min((int64_t)L, t0 + (int64_t)a.chunk) - t0) / kKeys);
+    if (early_tiles == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+  }
+  // this sequence's tree (T unless trees are ragged); read after the wait
+  int32_t Tb = early_tiles > 0 ? a.T : load_tree_size(a, b);
+  int64_t N = (int64_t)L + Tb;
+  int64_t t1 = min(N, t0 + a.chunk);
+  if (t0 >= t1) {  // nothing of this sequence falls in this chunk: an empty partial (both CTAs agree;
+                   // never taken by an early producer, whose chunk starts inside the prefix)
     if (rank == 0 && threadIdx.x < kRows && row0 + (int)threadIdx.x < R)
       a.part_lse[(int64_t)s * a.rows + (int64_t)b * R + row0 + threadIdx.x] = -INFINITY;
     return;
   }
-  const int ntiles = (int)((t1 - t0 + kKeys - 1) / kKeys);
+  int ntiles = (int)((t1 - t0 + kKeys - 1) / kKeys);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -313,15 +328,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_arrive_expect_tx(bar(kBarXFull + 0), kXBytes);  // first use of each exchange buffer
     mbar_arrive_expect_tx(bar(kBarXFull + 1), kXBytes);
   }
-  if (threadIdx.x < a.T) {  // tree parents of this sequence, validated, into shared memory
+  if (pidx >= 0 && pidx < a.T) {  // tree parents of this sequence, validated, into shared memory
     int p = par_raw;
-    if ((int)threadIdx.x >= Tb) {
+    if (pidx >= Tb) {
       p = -1;  // a padding node of a smaller tree
-    } else if (p < -1 || p >= (int)threadIdx.x) {
+    } else if (p < -1 || p >= pidx) {
       report(a.dev_status, a.debug, MLA_CHECK_BAD_PARENT);
       p = -1;
     }
-    s_parent[threadIdx.x] = p;
+    s_parent[pidx] = p;
   }
   if (warp == kSIssueWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -396,12 +411,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // (they are masked later).
     auto slot_at = [&](int64_t pos) -> int32_t { return pos < t1 ? (int32_t)slot_of(a, b, L, pos) : 0; };
     int64_t pbase = 0;  // hybrid addressing: slot of prefix position 0
-#pragma unroll
-    for (int j = 0; j < kStages; ++j) {
-      const int64_t pos = t0 + (int64_t)j * kKeys + row_base + (lane & 15);
-      if (a.hybrid) sr[j] = slot_at(pos);
-      else if (pos >= t1) sr[j] = 0;
-    }
     if (a.hybrid) {
       pbase = a.prefix_base[b];
       if (pbase < 0 || pbase + L > a.num_slots) {
@@ -410,74 +419,108 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
     const bool prefix_tiles_by_tma = a.hybrid && pbase + L <= a.num_slots && pbase + L < 0x7fffffffll;
+
+    // Tile t into stage j; sl_own is the slot of this lane's row of the tile.
+    auto issue_tile = [&](int t, int j, int32_t sl_own) {
+      const uint32_t sbase = base + j * kStageBytes;
+      const int64_t p0 = t0 + (int64_t)t * kKeys;
+      if (prefix_tiles_by_tma && p0 + kKeys <= L) {
+        // Hybrid addressing, a tile wholly inside the contiguous prefix: rows pbase + p0 ... + 63
+        // by 2-D TMA boxes that land in the same swizzled layouts (4 value blocks of 64 columns,
+        // then this CTA's 32 RoPE columns). One lane arms the stage with the byte count; every
+        // other producer lane arrives plainly, so the stage completes when the bytes land.
+        if (warp == 0 && lane == 0) {
+          const uint32_t full = bar(kBarKvFull + j);
+          mbar_arrive_expect_tx(full, kStageBytes);
+          const int y = (int)(pbase + p0);
+#pragma unroll
+          for (int vb = 0; vb < 4; ++vb)
+            asm volatile(
+                "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+                "%3}], [%4];" ::"r"(sbase + vb * kBlockBytes),
+                "l"(&tmap_kv), "r"((int)rank * 256 + vb * 64), "r"(y), "r"(full)
+                : "memory");
+          asm volatile(
+              "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+              "%3}], [%4];" ::"r"(sbase + 4 * kBlockBytes),
+              "l"(&tmap_rope), "r"(kDLatent + (int)rank * 32), "r"(y), "r"(full)
+              : "memory");
+        } else {
+          mbar_arrive(bar(kBarKvFull + j));
+        }
+        return;
+      }
+      if (sl_own < 0 || (int64_t)sl_own >= a.num_slots) {
+        report(a.dev_status, a.debug, MLA_CHECK_BAD_SLOT);
+        sl_own = sl_own < 0 ? 0 : (int32_t)min((int64_t)sl_own, a.num_slots - 1);
+      }
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {  // this CTA's 512 value bytes of one row per instruction
+        const int row = row_base + k;
+        const int64_t sl = __shfl_sync(0xffffffffu, sl_own, k);
+        const char* src = kvb + sl * (kDK * 2) + rank * 512 + lane * 16;
+        const uint32_t dst =
+            sbase + (lane >> 3) * kBlockBytes + row * 128 + ((((uint32_t)lane & 7u) ^ ((uint32_t)row & 7u)) << 4);
+        cp_async16(dst, src);
+      }
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {  // this CTA's 64 RoPE bytes of eight rows per instruction
+        const int kr = g * 8 + (lane >> 2);
+        const int row = row_base + kr;
+        const int64_t sl = __shfl_sync(0xffffffffu, sl_own, kr);
+        const char* src = kvb + sl * (kDK * 2) + 1024 + rank * 64 + (lane & 3) * 16;
+        const uint32_t dst = sbase + 4 * kBlockBytes + row * 64 +
+                             ((((uint32_t)lane & 3u) ^ (((uint32_t)row >> 1) & 3u)) << 4);
+        cp_async16(dst, src);
+      }
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar(kBarKvFull + j)) : "memory");
+    };
+
+    if (early_tiles > 0) {
+      // MLA_FLAG_PREFIX_STABLE: the first tiles lie wholly inside the prefix, whose length, slots
+      // and rows the preceding kernel does not write; they go out now, before that kernel has
+      // finished. Everything else (tree size, tree slots, later tiles) waits for it.
+#pragma unroll
+      for (int j = 0; j < kStages; ++j) {
+        if (j < early_tiles) {
+          const int64_t pos = t0 + (int64_t)j * kKeys + row_base + (lane & 15);  // < L
+          issue_tile(j, j, (int32_t)slot_of(a, b, L, pos));
+          if (warp == 0 && lane == 0 && j < 24) TRACE(14 + 10 * j);
+        }
+      }
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      Tb = load_tree_size(a, b);
+      N = (int64_t)L + Tb;
+      t1 = min(N, t0 + a.chunk);
+      ntiles = (int)((t1 - t0 + kKeys - 1) / kKeys);
+    }
+    // sr[j]: the slot for the next tile that uses stage j (tile j, or tile j + kStages when
+    // tile j already went out early). Slots prefetched before the wait are read again here when
+    // the early path was allowed (tree entries may have been rewritten by the preceding kernel).
+    const bool fresh_slots = a.hybrid || early_ok;
+#pragma unroll
+    for (int j = 0; j < kStages; ++j) {
+      const int64_t pos = t0 + (int64_t)(j < early_tiles ? j + kStages : j) * kKeys + row_base + (lane & 15);
+      if (fresh_slots) sr[j] = slot_at(pos);
+      else if (pos >= t1) sr[j] = 0;
+    }
     bool ok = true;
     for (int tb = 0; tb < ntiles && ok; tb += kStages) {
 #pragma unroll
       for (int j = 0; j < kStages; ++j) {
         const int t = tb + j;
         if (t >= ntiles) break;
-        const uint32_t sbase = base + j * kStageBytes;
+        if (t < early_tiles) continue;
         if (t >= kStages && !wait_warp(bar(kBarKvEmpty + j), ((t / kStages) - 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
-        int32_t sl_own = sr[j];
+        const int32_t sl_own = sr[j];
         {  // the slot of this lane's row of tile t + kStages, needed once this stage comes round again
           const int64_t pn = t0 + (int64_t)(t + kStages) * kKeys + row_base + (lane & 15);
-          sr[j] = a.hybrid ? slot_at(pn) : (pn < t1 ? tab[pn] : 0);
+          sr[j] = fresh_slots ? slot_at(pn) : (pn < t1 ? tab[pn] : 0);
         }
-        const int64_t p0 = t0 + (int64_t)t * kKeys;
-        if (prefix_tiles_by_tma && p0 + kKeys <= L) {
-          // Hybrid addressing, a tile wholly inside the contiguous prefix: rows pbase + p0 ... + 63
-          // by 2-D TMA boxes that land in the same swizzled layouts (4 value blocks of 64 columns,
-          // then this CTA's 32 RoPE columns). One lane arms the stage with the byte count; every
-          // other producer lane arrives plainly, so the stage completes when the bytes land.
-          if (warp == 0 && lane == 0) {
-            const uint32_t full = bar(kBarKvFull + j);
-            mbar_arrive_expect_tx(full, kStageBytes);
-            const int y = (int)(pbase + p0);
-#pragma unroll
-            for (int vb = 0; vb < 4; ++vb)
-              asm volatile(
-                  "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-                  "%3}], [%4];" ::"r"(sbase + vb * kBlockBytes),
-                  "l"(&tmap_kv), "r"((int)rank * 256 + vb * 64), "r"(y), "r"(full)
-                  : "memory");
-            asm volatile(
-                "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-                "%3}], [%4];" ::"r"(sbase + 4 * kBlockBytes),
-                "l"(&tmap_rope), "r"(kDLatent + (int)rank * 32), "r"(y), "r"(full)
-                : "memory");
-          } else {
-            mbar_arrive(bar(kBarKvFull + j));
-          }
-          if (warp == 0 && lane == 0 && t < 24) TRACE(14 + 10 * t);
-          continue;
-        }
-        if (sl_own < 0 || (int64_t)sl_own >= a.num_slots) {
-          report(a.dev_status, a.debug, MLA_CHECK_BAD_SLOT);
-          sl_own = sl_own < 0 ? 0 : (int32_t)min((int64_t)sl_own, a.num_slots - 1);
-        }
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {  // this CTA's 512 value bytes of one row per instruction
-          const int row = row_base + k;
-          const int64_t sl = __shfl_sync(0xffffffffu, sl_own, k);
-          const char* src = kvb + sl * (kDK * 2) + rank * 512 + lane * 16;
-          const uint32_t dst =
-              sbase + (lane >> 3) * kBlockBytes + row * 128 + ((((uint32_t)lane & 7u) ^ ((uint32_t)row & 7u)) << 4);
-          cp_async16(dst, src);
-        }
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {  // this CTA's 64 RoPE bytes of eight rows per instruction
-          const int kr = g * 8 + (lane >> 2);
-          const int row = row_base + kr;
-          const int64_t sl = __shfl_sync(0xffffffffu, sl_own, kr);
-          const char* src = kvb + sl * (kDK * 2) + 1024 + rank * 64 + (lane & 3) * 16;
-          const uint32_t dst = sbase + 4 * kBlockBytes + row * 64 +
-                               ((((uint32_t)lane & 3u) ^ (((uint32_t)row >> 1) & 3u)) << 4);
-          cp_async16(dst, src);
-        }
-        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar(kBarKvFull + j)) : "memory");
+        issue_tile(t, j, sl_own);
         if (warp == 0 && lane == 0 && t < 24) TRACE(14 + 10 * t);  // tile t's copies issued (warp 0)
       }
     }

@@ -473,7 +473,12 @@ def run_gpu(args):
     barrier()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
-        time.sleep(0.3)
+        # untimed replays while the sampler starts, so the timed replay begins at load clocks
+        t_end = time.time() + 0.3
+        while time.time() < t_end:
+            graph.replay()
+            torch.cuda.synchronize()
+        barrier()
         ev0.record(stream)
         graph.replay()
         ev1.record(stream)

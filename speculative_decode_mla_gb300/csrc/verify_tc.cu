@@ -91,14 +91,16 @@ static_assert(kTraceSlots >= 8 + 10 * 24 + 4, "trace slots");
 }  // namespace
 __device__ unsigned long long* g_mla_trace;
 namespace {
-__device__ __forceinline__ void trace_event(int slot) {
-  if (g_mla_trace != nullptr && slot < kTraceSlots) {
+// The buffer pointer is read once per thread at kernel start (trace_buf), so an event costs a
+// timer read and a store, not a global load on the path being timed.
+__device__ __forceinline__ void trace_event(unsigned long long* buf, int slot) {
+  if (buf != nullptr && slot < kTraceSlots) {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    g_mla_trace[(size_t)blockIdx.x * kTraceSlots + slot] = t;
+    buf[(size_t)blockIdx.x * kTraceSlots + slot] = t;
   }
 }
-#define TRACE(slot) trace_event(slot)
+#define TRACE(slot) trace_event(trace_buf, slot)
 #else
 #define TRACE(slot) ((void)0)
 #endif
@@ -130,18 +132,28 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      "{ .reg .pred p; mbarrier.try_wait.parity.relaxed.cluster.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
 // Bounded wait: false when another role aborted or the wait timed out (then it aborts).
+// cluster_scope: the phase is completed from the partner CTA (st.async bytes, remote arrive), a
+// release at cluster scope; it is polled relaxed and, once seen, acquired by one fence restricted
+// to shared::cluster memory, which is cheaper than an acquiring poll.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                          bool cluster_scope = false) {
   const long long start = clock64();
   while (true) {
-    if (cluster_scope ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
+    if (cluster_scope) {
+      if (mbar_test_cluster(bar, parity)) {
+        asm volatile("fence.acquire.sync_restrict::shared::cluster.cluster;" ::: "memory");
+        return true;
+      }
+    } else if (mbar_test(bar, parity)) {
+      return true;
+    }
     if (*abort_flag) return false;
     if (clock64() - start > kTimeoutCycles) {
       *abort_flag = 1;
@@ -230,6 +242,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     verify_tc_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap tmap_o,
                      const __grid_constant__ CUtensorMap tmap_kv, const __grid_constant__ CUtensorMap tmap_rope) {
   extern __shared__ uint8_t smem_raw[];
+#ifdef MLA_TC_TRACE
+  unsigned long long* const trace_buf = g_mla_trace;
+#endif
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw_addr);

@@ -12,11 +12,13 @@
 //                       out in order; a stage's barrier fires when its copies land
 //                       (cp.async.mbarrier.arrive.noinc), so no producer waits on its own
 //                       copies. One producer per warp scheduler keeps the issue load even.
-//   S issuer warp 4     S_r(t) = Q_r K_r^T over the CTA's 288 contraction dims into the TMEM
-//                       score buffer (tcgen05.mma kind::f16, fp32 accumulate; A = Q from
-//                       TMEM, B = K from the stage) once the softmax and the sender have
-//                       read S_r(t-1).
-//   PV issuer warp 5    O_r += P(t) V_r(t) (A = P from TMEM, B = the same stage read
+//   S issuer warp 4     S_r(t) = Q_r K_r^T over the CTA's 288 contraction dims into TMEM score
+//                       buffer t % 2 (tcgen05.mma kind::f16, fp32 accumulate; A = Q's 256
+//                       value dims from TMEM and its 32 RoPE dims from shared memory, B = K
+//                       from the stage) once the tile has landed and the softmax and the
+//                       sender have read S_r(t-2), so a tile's scores are computed while the
+//                       previous tile's are still being read and exchanged.
+//   PV issuer warp 5    O_r += P(t) V_r(t) (A = P from shared memory, B = the same stage read
 //                       MN-major, N = 256); its completion frees the stage.
 //   sender warps 11-14  as soon as S_r(t) is in TMEM, push it to the partner CTA through
 //                       distributed shared memory (st.async with a byte count on the
@@ -27,7 +29,9 @@
 //                       partial (S = S_0 + S_1), apply the ancestor bitmask on tree
 //                       positions, online softmax in the exp2 domain (O is rescaled only
 //                       when the running max grows by more than 2^8), write P (bf16) to
-//                       TMEM.
+//                       shared memory (128B-swizzled, the PV MMA's K-major A operand).
+//
+// TMEM (512 columns): O [0, 256), two S buffers [256, 384), Q's value dims [384, 512).
 //   release warp 6      tells the partner when this CTA has read a receive buffer.
 //   epilogue            O_r / l (fp16) goes through 128B-swizzled smem to TMA tensor
 //                       stores (rows past the sequence are clipped by the tensor map); lse
@@ -54,11 +58,14 @@ constexpr int kRopeBytes = kKeys * 64;              // 64 rows x 64 B: this CTA'
 constexpr int kStageBytes = 4 * kBlockBytes + kRopeBytes;  // 4 value blocks + the RoPE half
 constexpr int kXHalfBytes = kRows * kKeys * 2;      // fp16 partial scores of one tile
 constexpr int kXBytes = kXHalfBytes + kRows * 4;    // + one fp32 reference per row
-constexpr int kSmemX = kStages * kStageBytes;       // two exchange buffers follow the stages
+constexpr int kSmemP = kStages * kStageBytes;       // P (bf16, 128 rows x 64 positions, 128B swizzle)
+constexpr int kSmemQR = kSmemP + kRows * 128;       // the CTA's 32 RoPE dims of Q (128 rows x 64 B, 64B swizzle)
+constexpr int kSmemX = kSmemQR + kRows * 64;        // two exchange buffers
 constexpr int kSmemBar = kSmemX + 2 * kXBytes;
 constexpr int kSmemBytes = kSmemBar + 512 + 1024;   // barriers, TMEM slot, tree parents + alignment slack
 constexpr int kEpiBoxBytes = kRows * 128;           // one 64-column fp16 box of O (reuses the stages)
-static_assert(kStageBytes % 1024 == 0 && kSmemX % 16 == 0, "stage and exchange alignment");
+static_assert(kStageBytes % 1024 == 0 && kSmemP % 1024 == 0 && kSmemQR % 1024 == 0 && kSmemX % 16 == 0,
+              "stage, P, Q and exchange alignment");
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 constexpr int kProducerWarps = 4;  // warps 0..3, one per scheduler; warp p gathers rows 16p..16p+15 of each tile
@@ -71,13 +78,13 @@ constexpr int kThreads = 15 * 32;
 constexpr int kParentThread0 = kSIssueWarp * 32;  // threads reading the tree parents (T <= 64: warps 4-5)
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;  // O 256, S 64, P 32, Q 144 columns
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;  // O 256, two S buffers of 64, Q's 256 value dims 128
 
 // barrier indices (8 bytes each)
-constexpr int kBarKvFull = 0, kBarKvEmpty = kStages, kBarQFull = 2 * kStages, kBarSFull = kBarQFull + 1,
-              kBarSEmpty = kBarQFull + 2, kBarPFull = kBarQFull + 3, kBarPEmpty = kBarQFull + 4,
-              kBarXFull = kBarQFull + 5 /*2*/, kBarXEmpty = kBarQFull + 7 /*2*/, kBarXRead = kBarQFull + 9 /*2*/,
-              kBarDrainS = kBarQFull + 11, kBarDrainP = kBarQFull + 12, kNumBars = kBarQFull + 13;
+constexpr int kBarKvFull = 0, kBarKvEmpty = kStages, kBarQFull = 2 * kStages, kBarSFull = kBarQFull + 1 /*2*/,
+              kBarSEmpty = kBarQFull + 3 /*2*/, kBarPFull = kBarQFull + 5, kBarPEmpty = kBarQFull + 6,
+              kBarXFull = kBarQFull + 7 /*2*/, kBarXEmpty = kBarQFull + 9 /*2*/, kBarXRead = kBarQFull + 11 /*2*/,
+              kBarDrainS = kBarQFull + 13, kBarDrainP = kBarQFull + 14, kNumBars = kBarQFull + 15;
 static_assert(8 * kNumBars + 8 + 4 * kMaxNodes <= 512, "barrier area");
 
 constexpr long long kTimeoutCycles = 4000000000ll;  // ~2 s at 2 GHz
@@ -212,6 +219,29 @@ __device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uin
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+__device__ __forceinline__ void mma_smem_a(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Largest of a tile's kKeys scores, as eight interleaved chains (max is exact in any order).
+__device__ __forceinline__ float max_of_keys(const float* x) {
+  float m[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) m[u] = x[u];
+#pragma unroll
+  for (int k = 8; k < kKeys; k += 8)
+#pragma unroll
+    for (int u = 0; u < 8; ++u) m[u] = fmaxf(m[u], x[k + u]);
+  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint32_t* v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+               : "memory");
+}
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
@@ -327,8 +357,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarKvEmpty + i), 1);
     }
     mbar_init(bar(kBarQFull), 8);  // the softmax and the sender warps each stored their Q chunks
-    mbar_init(bar(kBarSFull), 1);
-    mbar_init(bar(kBarSEmpty), 8);  // the softmax and the sender warps have both read S
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kBarSFull + i), 1);
+      mbar_init(bar(kBarSEmpty + i), 8);  // the softmax and the sender warps have both read S buffer i
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarXFull + i), 1);   // armed locally with the exchange's byte count
       mbar_init(bar(kBarXEmpty + i), 1);  // one remote arrive from the partner's release warp per use
@@ -378,26 +410,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) TRACE(1);
 
   if (warp >= kSoftmaxWarp0) {
-    // Q -> TMEM, two bf16 per column: chunk c of the CTA's 36 (32 value, 4 RoPE) at column
-    // kColQ + 4c; the softmax warps store chunks 0-19, the sender warps chunks 20-35.
+    // Q: chunk c of the CTA's 32 value chunks at TMEM column kColQ + 4c (two bf16 per column),
+    // its 4 RoPE chunks in shared memory; the softmax warps store chunks 0-19, the sender warps
+    // chunks 20-35.
     const bool q_sender = warp >= kSenderWarp0;
     const int q_row = (warp & 3) * 32 + lane;  // tile row = TMEM lane of this thread
     const int q_c0 = q_sender ? 20 : 0, q_n = q_sender ? 16 : 20;
     const bool qvalid = row0 + q_row < R && (row0 + q_row) / a.H < Tb;
     const uint4* qrow = reinterpret_cast<const uint4*>(a.q + (qvalid ? (int64_t)b * R + row0 + q_row : 0) * kDK);
     uint32_t qv[80];
+    // two chunks (one 32-byte sector) per load, not kept in L1: each row is read once, and
+    // 16-byte pieces of 128 rows per warp would otherwise cycle through L1 eight times
 #pragma unroll
-    for (int i = 0; i < 20; ++i) {
-      const int chunk = q_c0 + i;
-      uint4 x = make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < 20; i += 2) {
+      const int chunk = q_c0 + i;  // even; a pair never straddles the value/RoPE boundary
+#pragma unroll
+      for (int k = 0; k < 8; ++k) qv[i * 4 + k] = 0u;
       if (qvalid && i < q_n) {
         const int src = chunk < 32 ? (int)rank * 32 + chunk : 64 + (int)rank * 4 + (chunk - 32);
-        x = __ldg(qrow + src);
+        asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                     : "=r"(qv[i * 4 + 0]), "=r"(qv[i * 4 + 1]), "=r"(qv[i * 4 + 2]), "=r"(qv[i * 4 + 3]),
+                       "=r"(qv[i * 4 + 4]), "=r"(qv[i * 4 + 5]), "=r"(qv[i * 4 + 6]), "=r"(qv[i * 4 + 7])
+                     : "l"(qrow + src));
       }
-      qv[i * 4 + 0] = x.x;
-      qv[i * 4 + 1] = x.y;
-      qv[i * 4 + 2] = x.z;
-      qv[i * 4 + 3] = x.w;
     }
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     if (!q_sender) {
@@ -405,7 +440,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 5; ++c) TMEM_ST16(lane_addr + kColQ + c * 16, (qv + c * 16));
     } else {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) TMEM_ST16(lane_addr + kColQ + 80 + c * 16, (qv + c * 16));
+      for (int c = 0; c < 3; ++c) TMEM_ST16(lane_addr + kColQ + 80 + c * 16, (qv + c * 16));
+      // RoPE chunks 32-35: row q_row of the 64B-swizzled K-major A operand of the RoPE K-steps
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        st_shared_v4(base + kSmemQR + q_row * 64 + (((uint32_t)c ^ (((uint32_t)q_row >> 1) & 3u)) << 4), qv + 48 + 4 * c);
+      fence_proxy_async();  // generic-proxy stores, read by the MMA (async proxy)
     }
     tmem_wait_st();
     tc_fence_before();
@@ -543,22 +583,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");  // this warp's setup phase
   } else if (warp == kSIssueWarp) {
     // ---------------------------------------------------------------- S issuer (one thread)
-    // S(t) = Q_r K_r^T over the CTA's 288 contraction dims (A = Q from TMEM, B = K from the
-    // stage) once tile t has landed and both readers are done with S(t-1).
+    // S(t) = Q_r K_r^T over the CTA's 288 contraction dims into S buffer t % 2 (A = Q, B = K from
+    // the stage) once tile t has landed and both readers are done with S(t-2) in that buffer.
     if (lane == 0) {
       constexpr uint32_t idesc_s = instr_desc(kRows, kKeys, 0);
       bool ok = wait_bar(bar(kBarQFull), 0, abort_flag);
       TRACE(4);
       for (int t = 0; t < ntiles && ok; ++t) {
+        const int sb = t & 1;  // S buffer of tile t
         ok = wait_bar(bar(kBarKvFull + t % kStages), (t / kStages) & 1, abort_flag);
-        if (ok && t >= 1) ok = wait_bar(bar(kBarSEmpty), (t - 1) & 1, abort_flag);
+        if (ok && t >= 2) ok = wait_bar(bar(kBarSEmpty + sb), ((t >> 1) - 1) & 1, abort_flag);
         if (!ok) break;
         if (t == 0) TRACE(5);
         // the stage was written by cp.async (generic proxy) and is read by the MMA (async proxy)
         fence_proxy_async();
         tc_fence_after();
         const uint32_t sbase = base + (t % kStages) * kStageBytes;
-        const uint32_t dS = tmem + kColS;
+        const uint32_t dS = tmem + kColS + (uint32_t)(sb * kKeys);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const uint64_t bd = smem_desc(sbase + (i >> 2) * kBlockBytes + (i & 3) * 32, 16, 1024);
@@ -566,10 +607,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {  // this CTA's half of the RoPE dims (64B-swizzled, 512 B per 8 rows)
+          const uint64_t ad = smem_desc(base + kSmemQR + kk * 32, 16, 512, 4);
           const uint64_t bd = smem_desc(sbase + 4 * kBlockBytes + kk * 32, 16, 512, 4);
-          mma_tmem_a(dS, tmem + kColQ + 128 + kk * 8, bd, idesc_s, 1u);
+          mma_smem_a(dS, ad, bd, idesc_s, 1u);
         }
-        mma_commit(bar(kBarSFull));
+        mma_commit(bar(kBarSFull + sb));
         if (t < 24) TRACE(16 + 10 * t);  // S(t) issued
       }
       // drain: every MMA this thread issued has completed once this barrier flips
@@ -593,8 +635,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t sbase = base + (t % kStages) * kStageBytes;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {  // 16 positions per step; V read MN-major from the same stage
+          const uint64_t ad = smem_desc(base + kSmemP + kk * 32, 16, 1024);
           const uint64_t bd = smem_desc(sbase + kk * 2048, kBlockBytes, 1024);
-          mma_tmem_a(tmem + kColO, tmem + kColP + kk * 8, bd, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+          mma_smem_a(tmem + kColO, ad, bd, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(bar(kBarKvEmpty + t % kStages));
         mma_commit(bar(kBarPEmpty));
@@ -632,23 +675,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t xfull_remote0 = map_to_cta(bar(kBarXFull), peer);
     for (int t = 0; t < ntiles; ++t) {
       const int xb = t & 1;
-      if (!wait_warp(bar(kBarSFull), t & 1, abort_flag)) break;
+      if (!wait_warp(bar(kBarSFull + xb), (t >> 1) & 1, abort_flag)) break;
       tc_fence_after();
       uint32_t su[kKeys];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) TMEM_LD16(lane_addr + kColS + c * 16, (su + c * 16));
+      for (int c = 0; c < 4; ++c) TMEM_LD16(lane_addr + kColS + xb * kKeys + c * 16, (su + c * 16));
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarSEmpty));
+      if (lane == 0) mbar_arrive(bar(kBarSEmpty + xb));
       // exp2-domain partial, as fp16 offsets from this row's largest partial among the keys
       // it can see in this tile (so the offsets of the keys that matter are small and exact
       // enough, and positions past the end never influence the result)
       float ref = -INFINITY;
       const int64_t p0 = t0 + (int64_t)t * kKeys;
       if (p0 + kKeys <= L) {
-#pragma unroll
-        for (int k = 0; k < kKeys; ++k) ref = fmaxf(ref, __uint_as_float(su[k]));
+        ref = max_of_keys(reinterpret_cast<const float*>(su));
       } else {
 #pragma unroll
         for (int k = 0; k < kKeys; ++k) {
@@ -704,19 +746,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int t = 0; t < ntiles && ok; ++t) {
       const int xb = t & 1;
-      if (!wait_warp(bar(kBarSFull), t & 1, abort_flag)) { ok = false; break; }
+      if (!wait_warp(bar(kBarSFull + xb), (t >> 1) & 1, abort_flag)) { ok = false; break; }
       if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(8 + 10 * t);
       tc_fence_after();
       float sc[kKeys];
       {
         uint32_t* su = reinterpret_cast<uint32_t*>(sc);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) TMEM_LD16(lane_addr + kColS + c * 16, (su + c * 16));
+        for (int c = 0; c < 4; ++c) TMEM_LD16(lane_addr + kColS + xb * kKeys + c * 16, (su + c * 16));
         tmem_wait_ld();
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarSEmpty));
+      if (lane == 0) mbar_arrive(bar(kBarSEmpty + xb));
       if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(9 + 10 * t);
 
       if (!wait_warp(bar(kBarXFull + xb), (t >> 1) & 1, abort_flag, true)) { ok = false; break; }
@@ -755,9 +797,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!vis) sc[k] = -INFINITY;
         }
       }
-      float mt = sc[0];
-#pragma unroll
-      for (int k = 1; k < kKeys; ++k) mt = fmaxf(mt, sc[k]);
+      const float mt = max_of_keys(sc);
       const float m_new = fmaxf(m_run, mt);
       bool rescale = false;
       float alpha = 1.f;
@@ -769,18 +809,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
       uint32_t pk[kKeys / 2];
-      float lsum = 0.f;
+      float lsum0 = 0.f, lsum1 = 0.f;  // two partial sums: shorter dependency chains
 #pragma unroll
       for (int k = 0; k < kKeys; k += 2) {
         const float e0 = ex2(sc[k] + neg_m);
         const float e1 = ex2(sc[k + 1] + neg_m);
-        const uint32_t pr = pack_bf16(e0, e1);
-        lsum += e0 + e1;
-        pk[k / 2] = pr;
+        pk[k / 2] = pack_bf16(e0, e1);
+        lsum0 += e0;
+        lsum1 += e1;
       }
-      l_run += lsum;
+      l_run += lsum0 + lsum1;
 
-      // P -> TMEM once PV of the previous tile has finished with it (and with O)
+      // P -> shared memory once PV of the previous tile has finished with it (and with O)
       if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(12 + 10 * t);
       if (t > 0) {
         if (!wait_warp(bar(kBarPEmpty), (t - 1) & 1, abort_flag)) { ok = false; break; }
@@ -800,8 +840,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           TMEM_ST16(lane_addr + kColO + c * 16, o);
         }
       }
-      TMEM_ST16(lane_addr + kColP, pk);
-      TMEM_ST16(lane_addr + kColP + 16, (pk + 16));
+      // P -> shared memory, the K-major A operand of the PV MMA: row r as eight 16-byte
+      // chunks of 8 positions, 128B-swizzled
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_shared_v4(base + kSmemP + r * 128 + (((uint32_t)c ^ ((uint32_t)r & 7u)) << 4), pk + 4 * c);
+      fence_proxy_async();  // generic-proxy stores, read by the MMA (async proxy)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

@@ -45,6 +45,8 @@
 #include <cuda_fp16.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace mla {
@@ -920,14 +922,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }  // namespace
 
 EncodeTiledFn tensor_map_encoder() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
+  // Looked up once per process; the initialiser of a function-local static runs in one thread
+  // while concurrent first callers wait for it.
+  static const EncodeTiledFn fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+      return reinterpret_cast<EncodeTiledFn>(p);
+    return static_cast<EncodeTiledFn>(nullptr);
+  }();
   return fn;
 }
 
@@ -940,14 +944,16 @@ extern "C" int mla_tc_trace_set(void* buffer) {
 #endif
 
 cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream) {
-  static bool configured[64] = {};  // the smem opt-in is set once per device
+  // the smem opt-in is set once per device (threads racing on the first call may both set it;
+  // setting it twice is harmless)
+  static std::atomic<bool> configured[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
+  if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev] = true;
+    if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   const int64_t units = (int64_t)a.B * a.row_tiles * a.splits;
   if (units * 2 > 0x7fffffff) return cudaErrorInvalidConfiguration;

@@ -55,7 +55,7 @@ def desc(**kw):
 def test_plan_64k_fills_the_gpu(lib):
     p = m.plan(desc(flags=0), 152)
     assert p.kernel == 0 and p.rows_per_tile == 128 and p.row_tiles == 1
-    assert p.chunk_tokens % 64 == 0
+    assert p.chunk_tokens % 64 == 0  # whole 64-position KV tiles
     assert p.num_splits * p.chunk_tokens >= 65552 > (p.num_splits - 1) * p.chunk_tokens
     assert 60 <= p.num_splits <= 76 and p.ctas == 2 * p.num_splits
     assert p.workspace_bytes >= p.num_splits * 128 * 512 * 2 + p.num_splits * 128 * 4

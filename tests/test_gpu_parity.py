@@ -37,14 +37,31 @@ def flags_of(name, debug=False):
 
 
 def sample_rows(p, per_seq=8, seed=0):
+    """Rows checked against the oracle on the full-size configs, stratified so that every part of
+    the kernel's row layout is compared: in every sequence, one row from each 32-row lane quarter
+    of each 128-row tile (the tensor-core kernel's TMEM lane groups), all heads of the first and
+    of the last node, and ``per_seq`` more drawn at random."""
     rng = np.random.default_rng(seed)
     R = p.T * p.H
     rows = []
     for b in range(p.B):
         pick = set(rng.choice(R, size=min(per_seq, R), replace=False).tolist())
-        pick |= {0, R - 1}
+        for q0 in range(0, R, 32):  # each lane quarter of each row tile
+            pick.add(int(rng.integers(q0, min(q0 + 32, R))))
+        pick |= set(range(min(p.H, R))) | set(range(R - p.H, R))
         rows += [b * R + r for r in sorted(pick)]
     return np.array(rows, dtype=np.int64)
+
+
+def test_sample_rows_cover_every_lane_quarter():
+    for name in ("wide", "185k", "batched"):
+        p = W.make_problem(name, with_kv=False)
+        R = p.T * p.H
+        rows = sample_rows(p, per_seq=4)
+        for b in range(p.B):
+            local = rows[(rows >= b * R) & (rows < (b + 1) * R)] - b * R
+            assert set(np.unique(local // 32)) == set(range((R + 31) // 32))
+            assert set(range(p.H)) <= set(local) and set(range(R - p.H, R)) <= set(local)
 
 
 # ------------------------------------------------------------------ named configs
@@ -78,7 +95,7 @@ def test_batched_sampled_rows(kernel):
 def test_wide_sampled_rows(kernel, cfg):
     p = W.make_problem(cfg)
     o, l = run(p, flags_of(kernel))
-    rows = sample_rows(p, per_seq=48)
+    rows = sample_rows(p, per_seq=16)
     ro, rl = oracle.verify_problem(p, SCALE, rows=rows)
     assert_close(o[rows], l[rows], ro, rl, cfg)
 
@@ -184,9 +201,12 @@ def test_constant_value_column_is_one(kernel):
     p.kv[:, 5] = one
     p.kv[:, 300] = one
     o, _ = run(p, flags_of(kernel), out_dtype=m.MLA_DTYPE_F32)
-    # SIMT: fp32 round-to-nearest sums. The tensor cores' fp32 accumulation of ~4000 bf16 terms
-    # drifts by up to about N * 2^-24 ~ 2.4e-4 relative, so the bar is set from that arithmetic.
-    tol = 1e-5 if kernel == "simt" else 2e-3
+    # Both kernels normalise O by the sum of the very weights the PV product used, so a constant
+    # column is 1 up to accumulation rounding: SIMT sums in fp32 (~1e-6). The tensor-core path adds
+    # (i) its fp32 accumulation of ~N = 4000 terms, at most N * 2^-24 ~ 2.4e-4 relative, and
+    # (ii) the fp16 rounding of each split's normalised partial, at most 2^-11 ~ 4.9e-4 near 1.0;
+    # (i) + (ii) ~ 7.3e-4 sets the bar at 1e-3.
+    tol = 1e-5 if kernel == "simt" else 1e-3
     assert np.abs(o[:, 5] - 1).max() < tol and np.abs(o[:, 300] - 1).max() < tol
 
 

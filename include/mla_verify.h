@@ -112,7 +112,7 @@ typedef struct mla_verify_desc {
 typedef struct mla_verify_plan_t {
   int32_t kernel;         /* 0: tcgen05 kernel, 1: SIMT reference kernel */
   int32_t num_splits;     /* KV partitions per (sequence, row tile); partial slots per row */
-  int32_t chunk_tokens;   /* positions per partition, a multiple of 64 */
+  int32_t chunk_tokens;   /* positions per partition, a multiple of 64 (the KV tile) */
   int32_t row_tiles;      /* row tiles per sequence */
   int32_t rows_per_tile;  /* query rows per tile */
   int32_t ctas;           /* CTAs launched by the attention kernel */
@@ -123,7 +123,7 @@ typedef struct mla_verify_plan_t {
  * mla_verify_plan -- the split plan for `desc` on a GPU with `num_sms` SMs.
  * Pure host function (no CUDA call; callable without a GPU). The KV range of
  * every sequence is cut into chunks of chunk_tokens positions (multiples of the
- * 64-token tile) so that the (sequence, row tile, chunk) units fill all SMs at
+ * 64-position KV tile) so that the (sequence, row tile, chunk) units fill all SMs at
  * batch 1 (split-KV / flash-decoding; the pages' batch-1 verify had "low
  * parallelism", "The Moment of Certainty", Message 12190: The Synthesis).
  * Returns MLA_OK or MLA_ERR_INVALID_ARGUMENT / MLA_ERR_UNSUPPORTED.
@@ -257,7 +257,9 @@ int mla_verify_combine(int32_t num_splits, int64_t rows, int32_t d_v, const void
  *
  * - Set-up: the first call on each device (with that device current) looks up
  *   the array's device address once and caches it. Make that first call before
- *   any stream capture begins on that device.
+ *   any stream capture begins on that device. The cached address is kept for
+ *   the life of the process, so resetting a device (cudaDeviceReset) after the
+ *   first call on it is not supported.
  * - Limit: when the plan for `desc` on the current device needs more than
  *   MLA_VERIFY_NOALLOC_SCRATCH_BYTES of workspace (see
  *   mla_verify_workspace_size), the call returns MLA_ERR_WORKSPACE_TOO_SMALL and
@@ -267,7 +269,10 @@ int mla_verify_combine(int32_t num_splits, int64_t rows, int32_t d_v, const void
  *   call writes every partial it reads), but two calls whose kernels overlap in
  *   time on the GPU (different streams without ordering between them) race on
  *   the array and corrupt each other's results. Order such calls on one stream
- *   or with events.
+ *   or with events. Calls ordered on one stream are safe back to back, also
+ *   with MLA_FLAG_PREFIX_STABLE: that flag lets a call read its prefix inputs
+ *   early, but its writes to the array (the split partials) still come after
+ *   it has waited for the preceding call's combine to finish.
  * Other arguments, return codes and behaviour are those of mla_verify_attn.
  */
 #define MLA_VERIFY_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20) /* 32 MiB */

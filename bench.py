@@ -13,8 +13,9 @@ e2e    = the same metric through the public call with host buffers: the step's i
 L2     = each step reads a different one of several distinct pools (together larger than L2).
 
 --impl reference times the float64 CPU oracle on this machine's host cores instead
-(the only other program that computes this operation here), on a bounded sample of
-rows per step, extrapolated to the full layer-step.
+(the only other program that computes this operation here): each step is one whole
+layer-step (all 128 query rows), or a stated row sample scaled to it when K + W whole
+steps would run past about two minutes.
 """
 import argparse
 import json
@@ -147,21 +148,32 @@ def traffic_record(fingerprint):
     return d.get("dram_bytes_per_launch")
 
 
-def cpu_baseline(p, rows_per_step, steps, warmup=0):
-    """Time the float64 oracle on ``rows_per_step`` rows per step; returns (seconds per full layer-step, threads)."""
+def cpu_baseline(p, steps, warmup=0, rows_per_step=None):
+    """Time the float64 oracle on this machine's host cores. Each step computes ``rows_per_step``
+    query rows (all rows of the layer-step by default) over their full visible sets. Returns
+    (seconds per full layer-step, OpenMP threads used, rows per step); with a row sample the time
+    is scaled to the full layer-step by rows / rows_per_step."""
     import oracle
     from speculative_decode_mla_gb300 import workloads as W
-    threads = oracle.max_threads()
+    n = p.rows if rows_per_step is None else min(p.rows, rows_per_step)
+    threads = min(oracle.max_threads(), n)
     rng = np.random.default_rng(0)
     times = []
     for it in range(warmup + steps):
-        rows = np.sort(rng.choice(p.rows, size=rows_per_step, replace=False))
+        rows = None if n == p.rows else np.sort(rng.choice(p.rows, size=n, replace=False))
         t0 = time.perf_counter()
         oracle.verify_problem(p, W.SOFTMAX_SCALE, rows=rows)
         dt = time.perf_counter() - t0
         if it >= warmup:
-            times.append(dt * p.rows / rows_per_step)
-    return float(np.mean(times)), min(threads, rows_per_step)
+            times.append(dt * p.rows / n)
+    return float(np.mean(times)), threads, n
+
+
+def bench_config(world):
+    """The workload description both arms print (the same dict for the GPU and the reference arm)."""
+    return {"workload": WORKLOAD, "batch": 1, "seq_len": 65536, "tree_nodes": 16, "heads": 8,
+            "parallelism": f"replicas x{world}" if world > 1 else "single",
+            "l2": f"inputs larger than L2: each step reads the next of {L2_ROTATION} distinct pools"}
 
 
 def run_reference(args):
@@ -171,18 +183,25 @@ def run_reference(args):
         return
     p = W.make_problem("64k")
     kv_bytes = W.kv_bytes_per_layer_step(p.seq_lens, p.T)
-    rows_per_step = 16
-    t_step, cores = cpu_baseline(p, rows_per_step, args.steps, args.warmup)
+    # one whole layer-step (all 128 query rows) per step, unless K + W such steps would not end
+    # within about two minutes: then a fixed row sample per step, scaled to the layer-step
+    t_one, _, _ = cpu_baseline(p, steps=1)
+    rows = None
+    if t_one * (args.steps + args.warmup) > 120.0:
+        rows = max(1, int(p.rows * 120.0 / (t_one * (args.steps + args.warmup))))
+    t_step, threads, n = cpu_baseline(p, args.steps, args.warmup, rows_per_step=rows)
     gbs = kv_bytes / t_step / 1e9
-    sample = (f"{rows_per_step} of {p.rows} query rows per step over the full 65552-position visible set, "
-              f"extrapolated x{p.rows // rows_per_step} to the layer-step")
+    if n == p.rows:
+        sample = f"each step is a whole layer-step: all {p.rows} query rows over the 65552-position visible set"
+    else:
+        sample = (f"{n} of {p.rows} query rows per step over the 65552-position visible set, "
+                  f"time scaled x{p.rows / n:.2f} to the layer-step")
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
             "us_per_layer_step": t_step * 1e6, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "batch": 1, "seq_len": 65536, "tree_nodes": 16, "heads": 8,
-                       "parallelism": "replicas"},
-            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "dtype": "f64", "data": "synthetic", "config": bench_config(world),
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "host_cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -606,9 +625,10 @@ def run_gpu(args):
 
     base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        t_cpu, cores = cpu_baseline(p, rows_per_step=min(p.rows, 32), steps=1)
-        base = {"value": kv_bytes / t_cpu / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                "sample": f"32 of {p.rows} query rows over the full visible set, extrapolated x{p.rows // 32}",
+        t_cpu, cores, _ = cpu_baseline(p, steps=2)
+        base = {"value": kv_bytes / t_cpu / 1e9, "unit": "GB/s", "cores": cores, "host_cores": os.cpu_count(),
+                "kind": "oracle",
+                "sample": f"2 whole layer-steps: all {p.rows} query rows over the 65552-position visible set",
                 "us_per_layer_step": t_cpu * 1e6}
     clocks = clk.summary()
     # the metric's own config also as a single isolated call (L2 flushed before it)
@@ -649,11 +669,9 @@ def run_gpu(args):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_s_max * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "batch": 1, "seq_len": 65536, "tree_nodes": 16, "heads": 8,
-                       "parallelism": "replicas" if world > 1 else "single",
-                       "l2": f"inputs larger than L2: each step reads the next of {L2_ROTATION} distinct pools",
-                       "kernel": "simt" if plan.kernel == 1 else "tcgen05", "splits": plan.num_splits,
-                       "chunk_tokens": plan.chunk_tokens},
+            "config": bench_config(world),
+            "plan": {"kernel": "simt" if plan.kernel == 1 else "tcgen05", "splits": plan.num_splits,
+                     "chunk_tokens": plan.chunk_tokens},
             "us_per_layer_step": step_s_max * 1e6,
             "hbm_frac_of_8tbs": value / world / NOMINAL_HBM_GBS,
             "hbm_frac_of_measured": value / world / peak_hbm,
@@ -687,6 +705,22 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_only(args):
+    """One named workload: 3 eager calls, then ``--steps`` calls replayed from a graph and 5 isolated
+    calls (see measure_config); prints one JSON line of its figures."""
+    import torch
+    import speculative_decode_mla_gb300 as m
+    from speculative_decode_mla_gb300 import _build
+    from speculative_decode_mla_gb300 import workloads as W
+    if args.only not in W.CONFIGS:
+        raise SystemExit(f"--only: unknown workload {args.only!r} (one of {', '.join(W.CONFIGS)})")
+    _build.build()
+    m.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    r = measure_config(m, W, dev, args.only, steps=args.steps)
+    print(json.dumps({"workload": args.only, **r}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -696,11 +730,20 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-185k", action="store_true", help="skip the 185k full-depth step measurement")
     ap.add_argument("--no-extra", action="store_true", help="skip the tiny/batched/wide timings")
+    ap.add_argument("--only", default=None,
+                    help="time one named workload alone (tiny, 64k, 185k = one of its layers, batched, wide, "
+                         "wide_identity) and print its figures; a small, self-contained case for profilers")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    world = dist_env()[1]
+    if args.gpus != world:
+        ap.error(f"--gpus {args.gpus} needs {args.gpus} processes, one per GPU (torchrun --nproc-per-node "
+                 f"{args.gpus}); this run has WORLD_SIZE={world}")
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        run_only(args)
     else:
         run_gpu(args)
 

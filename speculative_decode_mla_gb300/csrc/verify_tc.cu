@@ -58,16 +58,19 @@ constexpr int kStages = 4;              // KV stages in shared memory
 constexpr int kBlockBytes = kKeys * 128;            // 64 rows x 128 B (one 64-dim block, 128B swizzle)
 constexpr int kRopeBytes = kKeys * 64;              // 64 rows x 64 B: this CTA's 32 RoPE dims, 64B swizzle
 constexpr int kStageBytes = 4 * kBlockBytes + kRopeBytes;  // 4 value blocks + the RoPE half
-constexpr int kXHalfBytes = kRows * kKeys * 2;      // fp16 partial scores of one tile
-constexpr int kXBytes = kXHalfBytes + kRows * 4;    // + one fp32 reference per row
+constexpr int kXCodeBytes = kRows * kKeys * 2;      // 16-bit codes of the partial scores of one tile
+constexpr int kXBytes = kXCodeBytes + kRows * 8;    // + each row's reference and scale
 constexpr int kSmemP = kStages * kStageBytes;       // P (bf16, 128 rows x 64 positions, 128B swizzle)
 constexpr int kSmemQR = kSmemP + kRows * 128;       // the CTA's 32 RoPE dims of Q (128 rows x 64 B, 64B swizzle)
 constexpr int kSmemX = kSmemQR + kRows * 64;        // two exchange buffers
-constexpr int kSmemBar = kSmemX + 2 * kXBytes;
+constexpr int kSmemQV = kSmemX + 2 * kXBytes;       // Q's value dims 224..255 of this CTA (the same layout as QR)
+constexpr int kSmemOnes = kSmemQV + kRows * 64;     // 16 x 64 bf16 ones: the B operand of the row sums of P
+constexpr int kSmemBar = kSmemOnes + 16 * 128;
 constexpr int kSmemBytes = kSmemBar + 512 + 1024;   // barriers, TMEM slot, tree parents + alignment slack
 constexpr int kEpiBoxBytes = kRows * 128;           // one 64-column fp16 box of O (reuses the stages)
-static_assert(kStageBytes % 1024 == 0 && kSmemP % 1024 == 0 && kSmemQR % 1024 == 0 && kSmemX % 16 == 0,
-              "stage, P, Q and exchange alignment");
+static_assert(kStageBytes % 1024 == 0 && kSmemP % 1024 == 0 && kSmemQR % 1024 == 0 && kSmemX % 16 == 0 &&
+                  kXBytes % 16 == 0 && kSmemQV % 512 == 0 && kSmemOnes % 1024 == 0,
+              "stage, P, Q, exchange and ones alignment");
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 constexpr int kProducerWarps = 4;  // warps 0..3, one per scheduler; warp p gathers rows 16p..16p+15 of each tile
@@ -80,7 +83,9 @@ constexpr int kThreads = 15 * 32;
 constexpr int kParentThread0 = kSIssueWarp * 32;  // threads reading the tree parents (T <= 64: warps 4-5)
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;  // O 256, two S buffers of 64, Q's 256 value dims 128
+// O 256, two S buffers of 64, the row sums of P (16 identical columns), Q's value dims 0..223 (112)
+constexpr uint32_t kColO = 0, kColS = 256, kColL = 384, kColQ = 400;
+constexpr int kQTmemSteps = 14;  // K-steps of 16 value dims whose A operand is in TMEM
 
 // barrier indices (8 bytes each)
 constexpr int kBarKvFull = 0, kBarKvEmpty = kStages, kBarQFull = 2 * kStages, kBarSFull = kBarQFull + 1 /*2*/,
@@ -93,9 +98,11 @@ constexpr long long kTimeoutCycles = 4000000000ll;  // ~2 s at 2 GHz
 
 // Optional event timeline (built only with -DMLA_TC_TRACE): %globaltimer stamps of pipeline
 // events, kTraceSlots per CTA, into a buffer registered with mla_tc_trace_set.
-// 8 fixed events, then 10 per tile for the first 24 tiles (6 softmax, 2 producer, 2 MMA), then 4 at the end
+// 8 fixed events, then 13 per tile for the first 18 tiles (softmax, sender, producer, MMA), then 4 at
+// the end
 constexpr int kTraceSlots = 256;
-static_assert(kTraceSlots >= 8 + 10 * 24 + 4, "trace slots");
+constexpr int kTraceTiles = 18;
+static_assert(kTraceSlots >= 8 + 13 * kTraceTiles + 4, "trace slots");
 #ifdef MLA_TC_TRACE
 }  // namespace
 __device__ unsigned long long* g_mla_trace;
@@ -113,6 +120,8 @@ __device__ __forceinline__ void trace_event(unsigned long long* buf, int slot) {
 #else
 #define TRACE(slot) ((void)0)
 #endif
+#define TRACE_TILE(t, k) \
+  if ((t) < kTraceTiles) TRACE(8 + 13 * (t) + (k))
 
 // ------------------------------------------------------------------ PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -151,8 +160,18 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
 // cluster_scope: the phase is completed from the partner CTA (st.async bytes, remote arrive), a
 // release at cluster scope; it is polled relaxed and, once seen, acquired by one fence restricted
 // to shared::cluster memory, which is cheaper than an acquiring poll.
+// A probe of an mbarrier costs ~200 cycles even when the phase has completed, and so does reading
+// the clock: the first probe goes out before the clock is read.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                          bool cluster_scope = false) {
+  if (cluster_scope) {
+    if (mbar_test_cluster(bar, parity)) {
+      asm volatile("fence.acquire.sync_restrict::shared::cluster.cluster;" ::: "memory");
+      return true;
+    }
+  } else if (mbar_test(bar, parity)) {
+    return true;
+  }
   const long long start = clock64();
   while (true) {
     if (cluster_scope) {
@@ -238,6 +257,17 @@ __device__ __forceinline__ float max_of_keys(const float* x) {
   for (int k = 8; k < kKeys; k += 8)
 #pragma unroll
     for (int u = 0; u < 8; ++u) m[u] = fmaxf(m[u], x[k + u]);
+  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+}
+// Largest of the negated scores (the negated smallest score).
+__device__ __forceinline__ float max_of_neg_keys(const float* x) {
+  float m[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) m[u] = -x[u];
+#pragma unroll
+  for (int k = 8; k < kKeys; k += 8)
+#pragma unroll
+    for (int u = 0; u < 8; ++u) m[u] = fmaxf(m[u], -x[k + u]);
   return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint32_t* v) {
@@ -412,9 +442,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) TRACE(1);
 
   if (warp >= kSoftmaxWarp0) {
-    // Q: chunk c of the CTA's 32 value chunks at TMEM column kColQ + 4c (two bf16 per column),
-    // its 4 RoPE chunks in shared memory; the softmax warps store chunks 0-19, the sender warps
-    // chunks 20-35.
+    // Q: chunk c < 28 of the CTA's 32 value chunks (8 dims each) at TMEM column kColQ + 4c (two
+    // bf16 per column), chunks 28-31 and its 4 RoPE chunks in shared memory; the softmax warps
+    // store chunks 0-19, the sender warps chunks 20-35.
     const bool q_sender = warp >= kSenderWarp0;
     const int q_row = (warp & 3) * 32 + lane;  // tile row = TMEM lane of this thread
     const int q_c0 = q_sender ? 20 : 0, q_n = q_sender ? 16 : 20;
@@ -440,13 +470,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (!q_sender) {
 #pragma unroll
       for (int c = 0; c < 5; ++c) TMEM_ST16(lane_addr + kColQ + c * 16, (qv + c * 16));
+      // the ones operand of the row sums of P (bf16 1.0; 2 KB, 16 bytes per thread of warps 7-10)
+      reinterpret_cast<uint4*>(smem + kSmemOnes)[q_row] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+      fence_proxy_async();  // generic-proxy stores, read by the MMA (async proxy)
     } else {
 #pragma unroll
-      for (int c = 0; c < 3; ++c) TMEM_ST16(lane_addr + kColQ + 80 + c * 16, (qv + c * 16));
-      // RoPE chunks 32-35: row q_row of the 64B-swizzled K-major A operand of the RoPE K-steps
+      for (int c = 0; c < 2; ++c) TMEM_ST16(lane_addr + kColQ + 80 + c * 16, (qv + c * 16));
+      // value chunks 28-31 and RoPE chunks 32-35: row q_row of the 64B-swizzled K-major A operands
+      // of their K-steps
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        st_shared_v4(base + kSmemQR + q_row * 64 + (((uint32_t)c ^ (((uint32_t)q_row >> 1) & 3u)) << 4), qv + 48 + 4 * c);
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t off = q_row * 64 + (((uint32_t)c ^ (((uint32_t)q_row >> 1) & 3u)) << 4);
+        st_shared_v4(base + kSmemQV + off, qv + 32 + 4 * c);
+        st_shared_v4(base + kSmemQR + off, qv + 48 + 4 * c);
+      }
       fence_proxy_async();  // generic-proxy stores, read by the MMA (async proxy)
     }
     tmem_wait_st();
@@ -542,7 +579,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (j < early_tiles) {
           const int64_t pos = t0 + (int64_t)j * kKeys + row_base + (lane & 15);  // < L
           issue_tile(j, j, (int32_t)slot_of(a, b, L, pos));
-          if (warp == 0 && lane == 0 && j < 24) TRACE(14 + 10 * j);
+          if (warp == 0 && lane == 0) TRACE_TILE(j, 6);
         }
       }
       asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -578,7 +615,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           sr[j] = fresh_slots ? slot_at(pn) : (pn < t1 ? tab[pn] : 0);
         }
         issue_tile(t, j, sl_own);
-        if (warp == 0 && lane == 0 && t < 24) TRACE(14 + 10 * t);  // tile t's copies issued (warp 0)
+        if (warp == 0 && lane == 0) TRACE_TILE(t, 6);  // tile t's copies issued (warp 0)
       }
     }
     cp_async_wait_all();  // no copy may still be in flight when the CTA exits
@@ -605,7 +642,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const uint64_t bd = smem_desc(sbase + (i >> 2) * kBlockBytes + (i & 3) * 32, 16, 1024);
-          mma_tmem_a(dS, tmem + kColQ + i * 8, bd, idesc_s, i ? 1u : 0u);
+          if (i < kQTmemSteps)
+            mma_tmem_a(dS, tmem + kColQ + i * 8, bd, idesc_s, i ? 1u : 0u);
+          else  // value dims 224..255 (64B-swizzled, 512 B per 8 rows)
+            mma_smem_a(dS, smem_desc(base + kSmemQV + (i - kQTmemSteps) * 32, 16, 512, 4), bd, idesc_s, 1u);
         }
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {  // this CTA's half of the RoPE dims (64B-swizzled, 512 B per 8 rows)
@@ -614,7 +654,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mma_smem_a(dS, ad, bd, idesc_s, 1u);
         }
         mma_commit(bar(kBarSFull + sb));
-        if (t < 24) TRACE(16 + 10 * t);  // S(t) issued
+        TRACE_TILE(t, 8);  // S(t) issued
       }
       // drain: every MMA this thread issued has completed once this barrier flips
       mma_commit(bar(kBarDrainS));
@@ -629,6 +669,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // and the P columns.
     if (lane == 0) {
       constexpr uint32_t idesc_pv = instr_desc(kRows, 256, 1);
+      constexpr uint32_t idesc_l = instr_desc(kRows, 16, 0);
       bool ok = true;
       for (int t = 0; t < ntiles && ok; ++t) {
         ok = wait_bar(bar(kBarPFull), t & 1, abort_flag);
@@ -641,9 +682,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint64_t bd = smem_desc(sbase + kk * 2048, kBlockBytes, 1024);
           mma_smem_a(tmem + kColO, ad, bd, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
         }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // the row sums of P: B = 16 columns of ones
+          mma_smem_a(tmem + kColL, smem_desc(base + kSmemP + kk * 32, 16, 1024),
+                     smem_desc(base + kSmemOnes + kk * 32, 16, 1024), idesc_l, (t > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(kBarKvEmpty + t % kStages));
         mma_commit(bar(kBarPEmpty));
-        if (t < 24) TRACE(17 + 10 * t);  // PV(t) issued
+        TRACE_TILE(t, 9);  // PV(t) issued
       }
       mma_commit(bar(kBarDrainP));
       const long long st = clock64();
@@ -686,27 +731,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarSEmpty + xb));
-      // exp2-domain partial, as fp16 offsets from this row's largest partial among the keys
-      // it can see in this tile (so the offsets of the keys that matter are small and exact
-      // enough, and positions past the end never influence the result)
-      float ref = -INFINITY;
+      // The partial goes to the partner as 16-bit codes of a per-row fixed-point scale: hi is the
+      // row's largest partial among the keys it can see in this tile, s the smallest power of two
+      // with (hi - lowest such partial) / s <= 65535, and code = round((hi - p) / s), so the
+      // partner reads back hi - code * s with an error of at most s / 2. Positions past the end
+      // and tree positions the row cannot see stay out of the range (their codes saturate; they
+      // are masked later).
+      const float* sv = reinterpret_cast<const float*>(su);
+      float hi = -INFINITY, lo = INFINITY;
       const int64_t p0 = t0 + (int64_t)t * kKeys;
       if (p0 + kKeys <= L) {
-        ref = max_of_keys(reinterpret_cast<const float*>(su));
+        hi = max_of_keys(sv);
+        lo = -max_of_neg_keys(sv);
       } else {
 #pragma unroll
         for (int k = 0; k < kKeys; ++k) {
           const int64_t p = p0 + k;
-          if (p < L || (p < N && ((anc >> (p - L)) & 1ull))) ref = fmaxf(ref, __uint_as_float(su[k]));
+          if (p < L || (p < N && ((anc >> (p - L)) & 1ull))) {
+            hi = fmaxf(hi, sv[k]);
+            lo = fminf(lo, sv[k]);
+          }
         }
       }
-      ref = (ref == -INFINITY) ? 0.f : ref * a.scale_log2;  // softmax_scale > 0
+      if (!(hi >= lo)) hi = lo = 0.f;  // nothing visible (or a padding row)
+      const uint32_t xbits = __float_as_uint(fmaxf((hi - lo) * (1.f / 65535.f), 7.8886091e-31f));  // >= 2^-100
+      const uint32_t sbits = ((xbits & 0x7FFFFFu) ? xbits + 0x800000u : xbits) & 0x7F800000u;    // power of two
+      const float inv_step = __uint_as_float(0x7F000000u - sbits);                                  // 1 / s
       uint32_t hv[kKeys / 2];
 #pragma unroll
-      for (int k = 0; k < kKeys; k += 2) {
-        const __half2 h = __floats2half2_rn(fmaf(__uint_as_float(su[k]), a.scale_log2, -ref),
-                                            fmaf(__uint_as_float(su[k + 1]), a.scale_log2, -ref));
-        hv[k / 2] = *reinterpret_cast<const uint32_t*>(&h);
+      for (int k = 0; k < kKeys; k += 2) {  // round((hi - p) / s) in [0, 65535], by the 2^23 rounding trick
+        const float c0 = fminf(fmaxf((hi - sv[k]) * inv_step, 0.f), 65535.f) + 8388608.f;
+        const float c1 = fminf(fmaxf((hi - sv[k + 1]) * inv_step, 0.f), 65535.f) + 8388608.f;
+        hv[k / 2] = __byte_perm(__float_as_uint(c0), __float_as_uint(c1), 0x5410);
       }
       // the partner's buffer xb is free once it has read what this CTA sent there two tiles ago
       if (t >= 2 && !wait_warp(bar(kBarXEmpty + xb), ((t - 2) >> 1) & 1, abort_flag, true)) break;
@@ -720,11 +776,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             "r"(hv[4 * j]), "r"(hv[4 * j + 1]), "r"(hv[4 * j + 2]), "r"(hv[4 * j + 3]), "r"(xf)
             : "memory");
       }
-      asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
-                       xr + kXHalfBytes + r * 4),
-                   "r"(__float_as_uint(ref)), "r"(xf)
+      asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(
+                       xr + kXCodeBytes + r * 8),
+                   "r"(__float_as_uint(hi)), "r"(sbits), "r"(xf)
                    : "memory");
-      if (warp == kSenderWarp0 && lane == 0 && t < 24) TRACE(10 + 10 * t);
+      if (warp == kSenderWarp0 && lane == 0) TRACE_TILE(t, 2);
     }
   } else {
     // ---------------------------------------------------------------- softmax warps, one thread per row
@@ -743,13 +799,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int j = node, step = 0; j >= 0 && step < kMaxNodes; j = s_parent[j], ++step) anc |= 1ull << j;
     }
 
-    // l_run sums the exponentials (fp32, before P is rounded to bf16 for the MMA)
+    // l_run sums the exponentials in fp32 (it gives lse). O is normalised by the tensor cores' own
+    // row sums of the bf16 weights (TMEM columns kColL, a PV product with a ones matrix), so O / l
+    // is a convex combination of the values with exactly the weights used for them.
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int t = 0; t < ntiles && ok; ++t) {
       const int xb = t & 1;
       if (!wait_warp(bar(kBarSFull + xb), (t >> 1) & 1, abort_flag)) { ok = false; break; }
-      if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(8 + 10 * t);
+      if (warp == kSoftmaxWarp0 && lane == 0) TRACE_TILE(t, 0);
       tc_fence_after();
       float sc[kKeys];
       {
@@ -761,33 +819,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarSEmpty + xb));
-      if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(9 + 10 * t);
+      if (warp == kSoftmaxWarp0 && lane == 0) TRACE_TILE(t, 1);
 
       if (!wait_warp(bar(kBarXFull + xb), (t >> 1) & 1, abort_flag, true)) { ok = false; break; }
       if (warp == kSoftmaxWarp0 && lane == 0) {
-        if (t < 24) TRACE(11 + 10 * t);
+        TRACE_TILE(t, 3);
         mbar_arrive_expect_tx(bar(kBarXFull + xb), kXBytes);  // arm this buffer's next use
       }
-      // S (exp2 domain) = own partial * scale_log2 + partner's reference + partner's fp16 offset
+      // S (exp2 domain) = (own partial + partner's partial) * scale_log2, the partner's partial
+      // decoded as hi - code * s (its code bits placed over the exponent of 2^23 give 2^23 + code)
       {
         const uint8_t* xbuf = smem + kSmemX + xb * kXBytes;
-        const float pref = reinterpret_cast<const float*>(xbuf + kXHalfBytes)[r];
+        const uint2 hs = reinterpret_cast<const uint2*>(xbuf + kXCodeBytes)[r];
+        const float hi2 = __uint_as_float(hs.x) * a.scale_log2, step2 = __uint_as_float(hs.y) * a.scale_log2;
 #pragma unroll
         for (int j = 0; j < kKeys / 8; ++j) {
           const uint4 w = reinterpret_cast<const uint4*>(xbuf)[j * kRows + r];
           const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[u]));
+            const float c0 = __uint_as_float(__byte_perm(wv[u], 0x4B000000u, 0x7610)) - 8388608.f;
+            const float c1 = __uint_as_float(__byte_perm(wv[u], 0x4B000000u, 0x7632)) - 8388608.f;
             const int k = 8 * j + 2 * u;
-            sc[k] = fmaf(sc[k], a.scale_log2, f.x + pref);
-            sc[k + 1] = fmaf(sc[k + 1], a.scale_log2, f.y + pref);
+            sc[k] = fmaf(sc[k], a.scale_log2, fmaf(-c0, step2, hi2));
+            sc[k + 1] = fmaf(sc[k + 1], a.scale_log2, fmaf(-c1, step2, hi2));
           }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarXRead + xb));  // the release warp lets the partner refill it
-      if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(15 + 10 * t);
+      if (warp == kSoftmaxWarp0 && lane == 0) TRACE_TILE(t, 7);
 
       // tree positions (tail tiles only) and positions past the end are masked
       const int64_t p0 = t0 + (int64_t)t * kKeys;
@@ -823,7 +884,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       l_run += lsum0 + lsum1;
 
       // P -> shared memory once PV of the previous tile has finished with it (and with O)
-      if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(12 + 10 * t);
+      if (warp == kSoftmaxWarp0 && lane == 0) TRACE_TILE(t, 4);
       if (t > 0) {
         if (!wait_warp(bar(kBarPEmpty), (t - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -833,13 +894,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (__any_sync(0xffffffffu, rescale)) {
         const float f = rescale ? alpha : 1.f;
 #pragma unroll 1
-        for (int c = 0; c < 16; ++c) {
+        for (int c = 0; c <= 16; ++c) {  // O's 16 column blocks, then the row sums of P
+          const uint32_t col = c < 16 ? kColO + c * 16 : kColL;
           uint32_t o[16];
-          TMEM_LD16(lane_addr + kColO + c * 16, o);
+          TMEM_LD16(lane_addr + col, o);
           tmem_wait_ld();
 #pragma unroll
           for (int u = 0; u < 16; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * f);
-          TMEM_ST16(lane_addr + kColO + c * 16, o);
+          TMEM_ST16(lane_addr + col, o);
         }
       }
       // P -> shared memory, the K-major A operand of the PV MMA: row r as eight 16-byte
@@ -852,7 +914,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarPFull));
-      if (warp == kSoftmaxWarp0 && lane == 0 && t < 24) TRACE(13 + 10 * t);
+      if (warp == kSoftmaxWarp0 && lane == 0) TRACE_TILE(t, 5);
     }
 
     // epilogue: O_r / l through 128B-swizzled smem boxes (the stage buffers are idle now)
@@ -861,7 +923,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == kSoftmaxWarp0 && lane == 0) TRACE(kTraceSlots - 4);
     if (ok) {
       tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      uint32_t lr[16];
+      TMEM_LD16(lane_addr + kColL, lr);
+      tmem_wait_ld();
+      const float l_round = __uint_as_float(lr[0]);
+      const float inv = l_round > 0.f ? 1.f / l_round : 0.f;
       const int z = s * a.B + b;
       // Each warp owns its 32 rows (its TMEM lane quarter) of every box and stores them itself, so
       // the TMA store of box c overlaps the TMEM reads and conversion of box c + 1.

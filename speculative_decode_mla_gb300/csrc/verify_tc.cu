@@ -731,12 +731,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarSEmpty + xb));
-      // The partial goes to the partner as 16-bit codes of a per-row fixed-point scale: hi is the
-      // row's largest partial among the keys it can see in this tile, s the smallest power of two
-      // with (hi - lowest such partial) / s <= 65535, and code = round((hi - p) / s), so the
-      // partner reads back hi - code * s with an error of at most s / 2. Positions past the end
-      // and tree positions the row cannot see stay out of the range (their codes saturate; they
-      // are masked later).
+      // The partial goes to the partner as 16-bit codes on a per-row fixed-point grid. Over the
+      // keys the row can see in this tile, hi and lo are the largest and smallest partials; s is
+      // the smallest power of two with (hi - lo) / s <= 65534 and |hi| / s <= 2^22, n = ceil(hi / s),
+      // and a key's code is round(n - p / s), in [0, 65535]. The partner reads back
+      // n s - code s, exactly, so each partial it sees is off by at most s / 2. Positions past
+      // the end and tree positions the row cannot see stay out of the range; their codes are
+      // meaningless and they are masked later.
       const float* sv = reinterpret_cast<const float*>(su);
       float hi = -INFINITY, lo = INFINITY;
       const int64_t p0 = t0 + (int64_t)t * kKeys;
@@ -754,16 +755,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       if (!(hi >= lo)) hi = lo = 0.f;  // nothing visible (or a padding row)
-      const uint32_t xbits = __float_as_uint(fmaxf((hi - lo) * (1.f / 65535.f), 7.8886091e-31f));  // >= 2^-100
-      const uint32_t sbits = ((xbits & 0x7FFFFFu) ? xbits + 0x800000u : xbits) & 0x7F800000u;    // power of two
-      const float inv_step = __uint_as_float(0x7F000000u - sbits);                                  // 1 / s
+      const float span = fmaxf(fmaxf((hi - lo) * (1.f / 65534.f), fabsf(hi) * 2.38418579e-7f), 7.8886091e-31f);
+      const uint32_t xbits = __float_as_uint(span);
+      const uint32_t sbits = ((xbits & 0x7FFFFFu) ? xbits + 0x800000u : xbits) & 0x7F800000u;  // s, >= 2^-100
+      const float inv_step = __uint_as_float(0x7F000000u - sbits);                                // 1 / s
+      // 2^23 + n: an integer below 2^24, so exact, as is top = (2^23 + n) s
+      const float base = ceilf(hi * inv_step) + 8388608.f;
       uint32_t hv[kKeys / 2];
 #pragma unroll
-      for (int k = 0; k < kKeys; k += 2) {  // round((hi - p) / s) in [0, 65535], by the 2^23 rounding trick
-        const float c0 = fminf(fmaxf((hi - sv[k]) * inv_step, 0.f), 65535.f) + 8388608.f;
-        const float c1 = fminf(fmaxf((hi - sv[k + 1]) * inv_step, 0.f), 65535.f) + 8388608.f;
+      for (int k = 0; k < kKeys; k += 2) {
+        // 2^23 + n - p / s rounded once to fp32 lands on the integer 2^23 + code, whose low 16
+        // mantissa bits are the code
+        const float c0 = fmaf(-sv[k], inv_step, base);
+        const float c1 = fmaf(-sv[k + 1], inv_step, base);
         hv[k / 2] = __byte_perm(__float_as_uint(c0), __float_as_uint(c1), 0x5410);
       }
+      const float top = base * __uint_as_float(sbits);
       // the partner's buffer xb is free once it has read what this CTA sent there two tiles ago
       if (t >= 2 && !wait_warp(bar(kBarXEmpty + xb), ((t - 2) >> 1) & 1, abort_flag, true)) break;
       const uint32_t xr = x_remote0 + (uint32_t)(xb * kXBytes);
@@ -778,7 +785,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(
                        xr + kXCodeBytes + r * 8),
-                   "r"(__float_as_uint(hi)), "r"(sbits), "r"(xf)
+                   "r"(__float_as_uint(top)), "r"(sbits), "r"(xf)
                    : "memory");
       if (warp == kSenderWarp0 && lane == 0) TRACE_TILE(t, 2);
     }
@@ -826,23 +833,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         TRACE_TILE(t, 3);
         mbar_arrive_expect_tx(bar(kBarXFull + xb), kXBytes);  // arm this buffer's next use
       }
-      // S (exp2 domain) = (own partial + partner's partial) * scale_log2, the partner's partial
-      // decoded as hi - code * s (its code bits placed over the exponent of 2^23 give 2^23 + code)
+      // S = own partial + partner's partial (raw scores; the exp2-domain scale is applied in the
+      // exponent). A code's bits placed over the exponent of 2^23 read as c = 2^23 + code, and the
+      // partner's partial n s - code s is top - c s, exact in one fma (every term is an integer
+      // multiple of the power of two s, below 2^24 s in magnitude).
       {
         const uint8_t* xbuf = smem + kSmemX + xb * kXBytes;
         const uint2 hs = reinterpret_cast<const uint2*>(xbuf + kXCodeBytes)[r];
-        const float hi2 = __uint_as_float(hs.x) * a.scale_log2, step2 = __uint_as_float(hs.y) * a.scale_log2;
+        const float top = __uint_as_float(hs.x), step = __uint_as_float(hs.y);
 #pragma unroll
         for (int j = 0; j < kKeys / 8; ++j) {
           const uint4 w = reinterpret_cast<const uint4*>(xbuf)[j * kRows + r];
           const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const float c0 = __uint_as_float(__byte_perm(wv[u], 0x4B000000u, 0x7610)) - 8388608.f;
-            const float c1 = __uint_as_float(__byte_perm(wv[u], 0x4B000000u, 0x7632)) - 8388608.f;
+            const float c0 = __uint_as_float(__byte_perm(wv[u], 0x4B000000u, 0x7610));
+            const float c1 = __uint_as_float(__byte_perm(wv[u], 0x4B000000u, 0x7632));
             const int k = 8 * j + 2 * u;
-            sc[k] = fmaf(sc[k], a.scale_log2, fmaf(-c0, step2, hi2));
-            sc[k + 1] = fmaf(sc[k + 1], a.scale_log2, fmaf(-c1, step2, hi2));
+            sc[k] += fmaf(-c0, step, top);
+            sc[k + 1] += fmaf(-c1, step, top);
           }
         }
       }
@@ -860,7 +869,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!vis) sc[k] = -INFINITY;
         }
       }
-      const float mt = max_of_keys(sc);
+      const float mt = max_of_keys(sc) * a.scale_log2;  // exp2 domain (softmax_scale > 0)
       const float m_new = fmaxf(m_run, mt);
       bool rescale = false;
       float alpha = 1.f;
@@ -875,8 +884,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float lsum0 = 0.f, lsum1 = 0.f;  // two partial sums: shorter dependency chains
 #pragma unroll
       for (int k = 0; k < kKeys; k += 2) {
-        const float e0 = ex2(sc[k] + neg_m);
-        const float e1 = ex2(sc[k + 1] + neg_m);
+        const float e0 = ex2(fmaf(sc[k], a.scale_log2, neg_m));
+        const float e1 = ex2(fmaf(sc[k + 1], a.scale_log2, neg_m));
         pk[k / 2] = pack_bf16(e0, e1);
         lsum0 += e0;
         lsum1 += e1;

@@ -159,6 +159,9 @@ int run_splits(const mla_verify_desc* d, const void* q, const void* kv_pool, con
   a.tree_sizes = tree_sizes;
   a.hybrid = hybrid ? 1 : 0;
   a.early_prefix = (d->flags & MLA_FLAG_PREFIX_STABLE) ? 1 : 0;
+  // Several sequences: the tcgen05 kernel orders its units longest first from the lengths it
+  // reads after the programmatic-launch wait (so not with the early prefix gather).
+  a.lpt = (p.kernel == 0 && d->num_seqs >= 2 && d->num_seqs <= kLptMaxSeqs && !a.early_prefix) ? 1 : 0;
   a.seq_lens = seq_lens;
   a.tree_parent = tree_parent;
   a.part_o = static_cast<__half*>(workspace);

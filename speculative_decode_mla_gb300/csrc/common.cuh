@@ -16,6 +16,7 @@ constexpr int kDRope = 64;               // RoPE dims appended to each key row
 constexpr int kDK = kDLatent + kDRope;   // 576 bf16 = 1152 bytes per latent row
 constexpr int kTileTokens = 64;          // KV positions per tile; chunks are multiples of it
 constexpr int kMaxNodes = 64;            // tree nodes per sequence (one u64 ancestor mask)
+constexpr int kLptMaxSeqs = 64;          // longest-first unit order: up to two sequences per lane
 
 // Everything a kernel needs, by value (a kernel parameter).
 struct VerifyArgs {
@@ -37,6 +38,7 @@ struct VerifyArgs {
   int32_t debug;
   int32_t hybrid;     // 1: prefix_base / tree_slots addressing, 0: slot_table
   int32_t early_prefix;  // MLA_FLAG_PREFIX_STABLE: the prefix may be gathered before the preceding kernel ends
+  int32_t lpt;        // tcgen05 kernel, 2 <= B <= 64: work units in longest-first order (from the lengths)
   float scale;        // softmax scale
   float scale_log2;   // softmax scale * log2(e)
 };

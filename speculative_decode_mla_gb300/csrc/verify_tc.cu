@@ -13,30 +13,34 @@
 //                       (cp.async.mbarrier.arrive.noinc), so no producer waits on its own
 //                       copies. One producer per warp scheduler keeps the issue load even.
 //   S issuer warp 4     S_r(t) = Q_r K_r^T over the CTA's 288 contraction dims into TMEM score
-//                       buffer t % 2 (tcgen05.mma kind::f16, fp32 accumulate; A = Q's 256
-//                       value dims from TMEM and its 32 RoPE dims from shared memory, B = K
-//                       from the stage) once the tile has landed and the softmax and the
-//                       sender have read S_r(t-2), so a tile's scores are computed while the
-//                       previous tile's are still being read and exchanged.
+//                       buffer t % 2 (tcgen05.mma kind::f16, fp32 accumulate; A = Q's value
+//                       dims 0..223 from TMEM, its value dims 224..255 and 32 RoPE dims from
+//                       shared memory, B = K from the stage) once the tile has landed and the
+//                       softmax and the sender have read S_r(t-2), so a tile's scores are
+//                       computed while the previous tile's are still being read and exchanged.
 //   PV issuer warp 5    O_r += P(t) V_r(t) (A = P from shared memory, B = the same stage read
-//                       MN-major, N = 256); its completion frees the stage.
+//                       MN-major, N = 256), then l += P(t) 1 (N = 16 against a ones matrix:
+//                       the row sums of the bf16 weights, in TMEM); its completion frees the
+//                       stage.
 //   sender warps 11-14  as soon as S_r(t) is in TMEM, push it to the partner CTA through
 //                       distributed shared memory (st.async with a byte count on the
-//                       partner's mbarrier; two receive buffers per CTA). The partial
-//                       travels in the exp2 domain as fp16 offsets from a per-row fp32
-//                       reference (the row's largest visible partial in the tile).
+//                       partner's mbarrier; two receive buffers per CTA), as 16-bit codes on a
+//                       per-row power-of-two grid that the partner decodes exactly in one fma
+//                       (each partial off by at most half the grid step).
 //   softmax warps 7-10  one thread per query row: read S_r(t) from TMEM, add the partner's
 //                       partial (S = S_0 + S_1), apply the ancestor bitmask on tree
 //                       positions, online softmax in the exp2 domain (O is rescaled only
 //                       when the running max grows by more than 2^8), write P (bf16) to
 //                       shared memory (128B-swizzled, the PV MMA's K-major A operand).
-//
-// TMEM (512 columns): O [0, 256), two S buffers [256, 384), Q's value dims [384, 512).
 //   release warp 6      tells the partner when this CTA has read a receive buffer.
-//   epilogue            O_r / l (fp16) goes through 128B-swizzled smem to TMA tensor
-//                       stores (rows past the sequence are clipped by the tensor map); lse
-//                       to the split workspace. The combine kernel, launched as a
-//                       programmatic dependent, merges the splits.
+//   epilogue            O_r / l (fp16, l the tensor cores' row sum of the same bf16 weights)
+//                       goes through 128B-swizzled smem to TMA tensor stores (rows past the
+//                       sequence are clipped by the tensor map); lse (from the fp32 sum of the
+//                       unrounded exponentials) to the split workspace. The combine kernel,
+//                       launched as a programmatic dependent, merges the splits.
+//
+// TMEM (512 columns): O [0, 256), two S buffers [256, 384), l [384, 400), Q [400, 512).
+// A batch of 2..64 sequences takes its units longest first (lpt_unit), from the lengths.
 //
 // Every wait is bounded (about 2 s); on timeout the kernel stops issuing work,
 // drains what it started, reports MLA_CHECK_TIMEOUT in dev_status when given,
@@ -299,6 +303,93 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Inclusive prefix sum over the 64 values v0 (sequences 0..31, one per lane) and v1 (32..63).
+__device__ __forceinline__ void warp_scan64(int v0, int v1, int lane, int& inc0, int& inc1) {
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int u0 = __shfl_up_sync(0xffffffffu, v0, d), u1 = __shfl_up_sync(0xffffffffu, v1, d);
+    if (lane >= d) {
+      v0 += u0;
+      v1 += u1;
+    }
+  }
+  inc0 = v0;
+  inc1 = v1 + __shfl_sync(0xffffffffu, v0, 31);
+}
+// The first sequence whose inclusive prefix exceeds idx (-1 if none), and that prefix.
+__device__ __forceinline__ int first_above(int inc0, int inc1, int idx, int& inc_at) {
+  uint32_t m = __ballot_sync(0xffffffffu, inc0 > idx);
+  if (m) {
+    const int l = __ffs(m) - 1;
+    inc_at = __shfl_sync(0xffffffffu, inc0, l);
+    return l;
+  }
+  m = __ballot_sync(0xffffffffu, inc1 > idx);
+  const int l = m ? __ffs(m) - 1 : 0;
+  inc_at = __shfl_sync(0xffffffffu, inc1, l);
+  return m ? 32 + l : -1;
+}
+// Longest-first order of the work units of a batch of 2..64 sequences of different lengths, for
+// unit idx in [0, B x splits): every sequence's full chunks first (sequence by sequence), then
+// the partial last chunks from the longest down (equal lengths by sequence), then the (sequence,
+// split) pairs past a sequence's end, which only mark their partial empty. Clusters start in index
+// order, so the long units start first and the short ones fill the gaps at the end. Every lane of
+// the warp calls it; the result (sequence, split) is uniform across the warp.
+__device__ __forceinline__ void lpt_unit(const VerifyArgs& a, int idx, int lane, int& b_out, int& s_out) {
+  int full[2], part[2], nsp[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int bb = lane + 32 * i;
+    const int64_t n = bb < a.B ? (int64_t)load_len(a, bb) + load_tree_size(a, bb) : 0;
+    full[i] = (int)(n / a.chunk);
+    part[i] = (int)(n % a.chunk);
+    nsp[i] = full[i] + (part[i] > 0);
+  }
+  int inc0, inc1, at;
+  // 1. full chunks
+  warp_scan64(full[0], full[1], lane, inc0, inc1);
+  const int nfull = __shfl_sync(0xffffffffu, inc1, 31);
+  if (idx < nfull) {
+    const int bb = first_above(inc0, inc1, idx, at);
+    b_out = bb;
+    s_out = idx - (at - __shfl_sync(0xffffffffu, (bb >> 5) ? full[1] : full[0], bb & 31));
+    return;
+  }
+  idx -= nfull;
+  // 2. partial chunks, longest first: the one whose rank among the partial chunks is idx
+  const int npart = __popc(__ballot_sync(0xffffffffu, part[0] > 0)) + __popc(__ballot_sync(0xffffffffu, part[1] > 0));
+  if (idx < npart) {
+    int rank[2] = {0, 0};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll 4
+      for (int j = 0; j < 32; ++j) {
+        const int pj = __shfl_sync(0xffffffffu, part[h], j);
+        const int bj = 32 * h + j;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int bi = lane + 32 * i;
+          rank[i] += (pj > part[i] || (pj == part[i] && bj < bi)) && pj > 0;
+        }
+      }
+    }
+    const uint32_t m0 = __ballot_sync(0xffffffffu, part[0] > 0 && rank[0] == idx);
+    const uint32_t m1 = __ballot_sync(0xffffffffu, part[1] > 0 && rank[1] == idx);
+    const int bb = m0 ? __ffs(m0) - 1 : 32 + __ffs(m1) - 1;
+    b_out = bb;
+    s_out = __shfl_sync(0xffffffffu, (bb >> 5) ? full[1] : full[0], bb & 31);
+    return;
+  }
+  idx -= npart;
+  // 3. splits past each sequence's end
+  warp_scan64(lane < a.B ? a.splits - nsp[0] : 0, lane + 32 < a.B ? a.splits - nsp[1] : 0, lane, inc0, inc1);
+  const int bb = first_above(inc0, inc1, idx, at);
+  const int bsafe = bb < 0 ? 0 : bb;  // (idx < B x splits always finds one)
+  const int emp = a.splits - __shfl_sync(0xffffffffu, (bsafe >> 5) ? nsp[1] : nsp[0], bsafe & 31);
+  b_out = bsafe;
+  s_out = a.splits - emp + (idx - (at - emp));
+}
+
 // ------------------------------------------------------------------ the kernel
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     verify_tc_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap tmap_o,
@@ -325,21 +416,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t peer = rank ^ 1u;
 
   // which unit
+  // which unit: (split, row tile, sequence) from the index, or, for a batch in longest-first
+  // order, the row tile from the index and the (sequence, split) from the lengths after the wait
   const int unit = blockIdx.x >> 1;
-  const int s = unit % a.splits;
-  const int bt = unit / a.splits;
-  const int tile_idx = bt % a.row_tiles;
-  const int b = bt / a.row_tiles;
+  int s, tile_idx, b;
+  if (a.lpt) {
+    tile_idx = unit % a.row_tiles;
+    s = b = 0;
+  } else {
+    s = unit % a.splits;
+    const int bt = unit / a.splits;
+    tile_idx = bt % a.row_tiles;
+    b = bt / a.row_tiles;
+  }
   const int R = a.T * a.H;
   const int row0 = tile_idx * kRows;
-  const int64_t t0 = (int64_t)s * a.chunk;
   // Launched as a programmatic dependent: everything above read no global memory; from here on
   // the inputs may have been written by the kernel before this one in the stream. With
   // MLA_FLAG_PREFIX_STABLE the producer warps may read the prefix (length, slots, rows) first and
   // wait just before anything else (see the producer section).
   const bool producer = warp < kProducerWarps;
-  const bool early_ok = a.early_prefix && producer;
+  const bool early_ok = a.early_prefix && producer;  // (never with the longest-first order)
   if (!early_ok) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (a.lpt) lpt_unit(a, unit / a.row_tiles, lane, b, s);
+  const int64_t t0 = (int64_t)s * a.chunk;
 
   // The reads the set-up waits on are issued together, before anything waits on one: the slots
   // of the first kStages tiles (producer warp), the prefix length and the tree parents. The query

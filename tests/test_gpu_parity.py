@@ -140,11 +140,13 @@ SHAPES = [
     ([77, 300], 3, 5, "star"),      # rows per sequence not a multiple of 8 / 128
     ([2000], 16, 8, "chain"),       # chain tree: causal tail
     ([5000, 4500, 6000], 9, 13, "random"),  # several tiles and a ragged tail per sequence
+    ([(i * 53) % 700 for i in range(64)], 3, 4, "random"),  # 64 sequences: the longest-first unit order
+    ([(i * 97) % 900 for i in range(70)], 2, 2, "random"),  # 70 sequences: units in index order
 ]
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-@pytest.mark.parametrize("shape", SHAPES, ids=[f"L{s[0]}-T{s[1]}-H{s[2]}-{s[3]}" for s in SHAPES])
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"B{len(s[0])}-L{max(s[0])}-T{s[1]}-H{s[2]}-{s[3]}" for s in SHAPES])
 def test_shapes(kernel, shape):
     lens, T, H, tree = shape
     p = W.custom_problem(lens, T, H, tree=tree, seed=len(lens) * 100 + T + H, pool_slack=37, stride_pad=5)

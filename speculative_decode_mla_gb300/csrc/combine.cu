@@ -26,6 +26,9 @@ constexpr int kCols = 128;       // columns per CTA (32 lanes x 4)
 constexpr int kWarps = 8;
 constexpr int kBatch = 10;       // splits per warp whose loads are in flight together (plain kernel)
 constexpr int kTmaSplits = 128;  // splits per TMA box (32 KB of shared memory)
+// From this many (row, 128-column) items on, one warp per item instead of one CTA (more than
+// one wave of 8-warp CTAs on this part's SMs).
+constexpr int64_t kWarpKernelItems = 2048;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kTimeoutCycles = 4000000000ll;  // ~2 s at 2 GHz
 
@@ -61,6 +64,29 @@ __device__ __forceinline__ void fold(float ls, float M, float4 v, float& z, floa
   acc.w = fmaf(w, v.w, acc.w);
 }
 
+// Writes a row's 4 columns at c, O = acc / Z, and (write_lse) its lse = M + ln Z.
+__device__ __forceinline__ void store_row(float M, float Z, float4 t, int64_t r, int c, int32_t d_v, void* out,
+                                          float* lse, int32_t out_dtype, bool write_lse) {
+  const float inv = Z > 0.f ? 1.f / Z : 0.f;  // all parts empty: out = 0, lse = -inf
+  t.x *= inv;
+  t.y *= inv;
+  t.z *= inv;
+  t.w *= inv;
+  if (c < d_v) {
+    if (out_dtype == MLA_DTYPE_F32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(out) + r * d_v + c) = t;
+    } else {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(t.x, t.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(t.z, t.w);
+      uint2 packed;
+      packed.x = *reinterpret_cast<uint32_t*>(&lo);
+      packed.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + r * d_v + c) = packed;
+    }
+  }
+  if (write_lse && lse) lse[r] = (Z > 0.f || Z != Z) ? M + logf(Z) : -INFINITY;
+}
+
 // Sums the warps' (z, acc) and writes the row's 128 columns and its lse (warp 0 does the writing).
 __device__ __forceinline__ void finish(float M, float z, float4 acc, int64_t r, int c, int32_t d_v, void* out,
                                        float* lse, int32_t out_dtype, int warp, int lane) {
@@ -81,24 +107,7 @@ __device__ __forceinline__ void finish(float M, float z, float4 acc, int64_t r, 
     t.z += x.z;
     t.w += x.w;
   }
-  const float inv = Z > 0.f ? 1.f / Z : 0.f;  // all parts empty: out = 0, lse = -inf
-  t.x *= inv;
-  t.y *= inv;
-  t.z *= inv;
-  t.w *= inv;
-  if (c < d_v) {
-    if (out_dtype == MLA_DTYPE_F32) {
-      *reinterpret_cast<float4*>(static_cast<float*>(out) + r * d_v + c) = t;
-    } else {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(t.x, t.y);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(t.z, t.w);
-      uint2 packed;
-      packed.x = *reinterpret_cast<uint32_t*>(&lo);
-      packed.y = *reinterpret_cast<uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + r * d_v + c) = packed;
-    }
-  }
-  if (lane == 0 && blockIdx.y == 0 && lse) lse[r] = (Z > 0.f || Z != Z) ? M + logf(Z) : -INFINITY;
+  store_row(M, Z, t, r, c, d_v, out, lse, out_dtype, lane == 0 && blockIdx.y == 0);
 }
 
 template <typename PT>
@@ -124,8 +133,8 @@ combine_kernel(int32_t splits, int64_t rows, int32_t d_v, const PT* __restrict__
     for (int u = 0; u < kBatch; ++u) {
       const int sp = s0 + u * kWarps;
       ls[u] = sp < splits ? part_lse[(int64_t)sp * rows + r] : -INFINITY;
-      v[u] = (sp < splits && col_ok) ? load4(part_o + ((int64_t)sp * rows + r) * d_v + c)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[u] = (sp < splits && col_ok && ls[u] != -INFINITY) ? load4(part_o + ((int64_t)sp * rows + r) * d_v + c)
+                                                            : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u)
@@ -221,6 +230,71 @@ combine_tma_kernel(const __grid_constant__ CUtensorMap tm, int32_t splits, int32
   finish(M, z, acc, r, c0 + lane * 4, d_v, out, lse, out_dtype, warp, lane);
 }
 
+// Many rows (batches of sequences, wide head counts): one warp per (row, 128 columns), eight per
+// CTA. A CTA per row would spend its time on launch and load latency, wave after wave, for the
+// few splits a row of a batch has; here a warp reads the row's lse values, then only the splits
+// up to the last non-empty one, eight loads in flight per lane. The folds keep one (z, acc) per
+// residue of the split index mod 8 and add them in that order, the order in which the CTA
+// kernels' eight warps fold and are summed, so every combine kernel gives the same bits.
+template <typename PT>
+__global__ void __launch_bounds__(kWarps * 32)
+combine_warp_kernel(int32_t splits, int64_t rows, int32_t d_v, int32_t col_blocks, const PT* __restrict__ part_o,
+                    const float* __restrict__ part_lse, void* __restrict__ out, float* __restrict__ lse,
+                    int32_t out_dtype) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // no-op unless launched as a dependent
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t item = (int64_t)blockIdx.x * kWarps + warp;
+  if (item >= rows * col_blocks) return;  // (no block-wide synchronisation below)
+  const int64_t r = item / col_blocks;
+  const int cb = (int)(item % col_blocks);
+  const int c = cb * kCols + lane * 4;
+  const bool col_ok = c < d_v;
+  float M = -INFINITY;
+  int last = -1;
+  for (int s = lane; s < splits; s += 32) {
+    const float l = part_lse[(int64_t)s * rows + r];
+    M = fmaxf(M, l);
+    if (l != -INFINITY) last = s;  // (a NaN counts: it must reach the output)
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+  }
+  float z[kWarps];
+  float4 acc[kWarps];
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    z[w] = 0.f;
+    acc[w] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int s0 = 0; s0 <= last; s0 += kWarps) {
+    float ls[kWarps];
+    float4 v[kWarps];
+#pragma unroll
+    for (int u = 0; u < kWarps; ++u) ls[u] = s0 + u <= last ? part_lse[(int64_t)(s0 + u) * rows + r] : -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kWarps; ++u)
+      v[u] = (col_ok && ls[u] != -INFINITY) ? load4(part_o + ((int64_t)(s0 + u) * rows + r) * d_v + c)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < kWarps; ++u)
+      if (ls[u] != -INFINITY) fold(ls[u], M, v[u], z[u], acc[u]);
+  }
+  float Z = 0.f;
+  float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    Z += z[w];
+    t.x += acc[w].x;
+    t.y += acc[w].y;
+    t.z += acc[w].z;
+    t.w += acc[w].w;
+  }
+  store_row(M, Z, t, r, c, d_v, out, lse, out_dtype, lane == 0 && cb == 0);
+}
+
 }  // namespace
 
 cudaError_t launch_combine(int32_t splits, int64_t rows, int32_t d_v, const void* part_o, int32_t part_dtype,
@@ -237,6 +311,15 @@ cudaError_t launch_combine(int32_t splits, int64_t rows, int32_t d_v, const void
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = dependent ? 1 : 0;
+  const int32_t col_blocks = (d_v + kCols - 1) / kCols;
+  if ((int64_t)rows * col_blocks >= kWarpKernelItems) {
+    cfg.gridDim = dim3((unsigned)(((int64_t)rows * col_blocks + kWarps - 1) / kWarps));
+    if (part_dtype == MLA_DTYPE_F16)
+      return cudaLaunchKernelEx(&cfg, combine_warp_kernel<__half>, splits, rows, d_v, col_blocks,
+                                static_cast<const __half*>(part_o), part_lse, out, lse, out_dtype);
+    return cudaLaunchKernelEx(&cfg, combine_warp_kernel<float>, splits, rows, d_v, col_blocks,
+                              static_cast<const float*>(part_o), part_lse, out, lse, out_dtype);
+  }
   EncodeTiledFn enc = tensor_map_encoder();
   if (part_dtype == MLA_DTYPE_F16 && d_v % kCols == 0 && enc != nullptr &&
       (reinterpret_cast<uintptr_t>(part_o) & 15) == 0 && rows <= 0x7fffffff && splits <= 0x7fffffff) {

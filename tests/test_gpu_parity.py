@@ -305,6 +305,35 @@ def test_combine_entry_point_matches_oracle_combine():
     assert_close(o.cpu().numpy().astype(np.float64), l.cpu().numpy(), full_o, full_l, "combine")
 
 
+@pytest.mark.parametrize("dtype", ["f16", "f32"])
+def test_combine_many_rows_same_bits_as_few_rows(dtype):
+    """From 2048 (row, 128-column) items on, the combine runs one warp per item instead of one CTA
+    per row; it folds the splits in the same order, so a row's result carries the same bits
+    whichever kernel ran it. Checked on seeded partials with empty splits (lse = -inf) at the end
+    of some rows, as a batch of sequences of different lengths leaves them, and against the
+    oracle's combine."""
+    import torch
+    import speculative_decode_mla_gb300 as m
+    rng = np.random.default_rng(83)
+    splits, rows, d_v = 11, 700, 512  # 700 x 4 column blocks = 2800 items: the per-warp kernel
+    po = rng.standard_normal((splits, rows, d_v)).astype(np.float32)
+    pl = (rng.standard_normal((splits, rows)) * 3.0).astype(np.float32)
+    nsp = rng.integers(1, splits + 1, size=rows)  # row r has splits [0, nsp[r]) with positions
+    pl[np.arange(splits)[:, None] >= nsp[None, :]] = -np.inf
+    pt = np.float16 if dtype == "f16" else np.float32
+    big_o, big_l = m.combine(torch.from_numpy(po.astype(pt)).cuda(), torch.from_numpy(pl).cuda(),
+                             out_dtype=m.MLA_DTYPE_F32)
+    few = 100  # 400 items: one CTA per row
+    sm_o, sm_l = m.combine(torch.from_numpy(np.ascontiguousarray(po[:, :few].astype(pt))).cuda(),
+                           torch.from_numpy(np.ascontiguousarray(pl[:, :few])).cuda(), out_dtype=m.MLA_DTYPE_F32)
+    torch.cuda.synchronize()
+    assert np.array_equal(big_o.cpu().numpy()[:few], sm_o.cpu().numpy())
+    assert np.array_equal(big_l.cpu().numpy()[:few], sm_l.cpu().numpy())
+    ro, rl = oracle.combine(po.astype(pt).astype(np.float64), pl.astype(np.float64))
+    assert np.abs(big_o.cpu().numpy() - ro).max() < 1e-5 * max(1.0, np.abs(po).max())
+    assert np.abs(big_l.cpu().numpy() - rl).max() < 1e-5 * max(1.0, np.abs(rl).max())
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_partials_then_combine_equals_attn(kernel):
     """mla_verify_attn_partials + mla_verify_combine on its workspace is bit-identical to mla_verify_attn."""

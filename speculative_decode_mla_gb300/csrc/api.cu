@@ -61,6 +61,13 @@ extern "C" int mla_verify_plan(const mla_verify_desc* d, int32_t num_sms, mla_ve
   int64_t best_tiles = 1;
   if (d->num_splits > 0) {
     best_tiles = cdiv(max_tiles, d->num_splits);
+  } else if (ragged && !simt && d->num_seqs <= kLptMaxSeqs) {
+    // A batch of different lengths whose units run longest first: the chunk is the clusters'
+    // even share of all tiles, so the full chunks never outnumber the cluster slots, and the
+    // shorter last chunks fill the slots as they free.
+    const int64_t share = cdiv(cdiv(total, kTileTokens) * p.row_tiles, slots);
+    best_tiles = share < 1 ? 1 : (share > max_tiles ? max_tiles : share);
+    if (cdiv(max_tiles, best_tiles) > kMaxSplits) best_tiles = cdiv(max_tiles, kMaxSplits);
   } else {
     // Pick the chunk (in 64-token tiles) that minimises the estimated makespan:
     // waves of units x (tiles per chunk + a fixed per-unit cost of ~4 tiles for the

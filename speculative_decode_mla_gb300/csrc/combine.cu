@@ -15,6 +15,8 @@
 // fp16 partials with d_v a multiple of 128 arrive by one TMA tensor load per CTA (a box
 // of 128 columns x 1 row x up to 128 splits), which also keeps them off the per-SM limit
 // on outstanding LSU requests; fp32 partials are read with plain vector loads.
+// Calls with many rows (batches, wide head counts) use one warp per (row, 128 columns)
+// instead, which folds in the same order (combine_warp_kernel).
 // Launched after the attention kernel with programmatic dependent launch: the kernel
 // waits for the primary grid's results before its first read.
 #include "common.cuh"

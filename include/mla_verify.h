@@ -126,6 +126,10 @@ typedef struct mla_verify_plan_t {
  * 64-position KV tile) so that the (sequence, row tile, chunk) units fill all SMs at
  * batch 1 (split-KV / flash-decoding; the pages' batch-1 verify had "low
  * parallelism", "The Moment of Certainty", Message 12190: The Synthesis).
+ * For a batch of 2..64 sequences whose total_tokens_hint is below B x the longest
+ * (lengths differ), the tcgen05 kernel takes its units longest first, and the
+ * chunk is the cluster slots' even share of all tiles. The hint only sizes the
+ * plan: any lengths give correct results.
  * Returns MLA_OK or MLA_ERR_INVALID_ARGUMENT / MLA_ERR_UNSUPPORTED.
  */
 int mla_verify_plan(const mla_verify_desc *desc, int32_t num_sms, mla_verify_plan_t *plan);

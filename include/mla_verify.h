@@ -126,8 +126,8 @@ typedef struct mla_verify_plan_t {
  * 64-position KV tile) so that the (sequence, row tile, chunk) units fill all SMs at
  * batch 1 (split-KV / flash-decoding; the pages' batch-1 verify had "low
  * parallelism", "The Moment of Certainty", Message 12190: The Synthesis).
- * For a batch of 2..64 sequences whose total_tokens_hint is below B x the longest
- * (lengths differ), the tcgen05 kernel takes its units longest first, and the
+ * For a batch of 2..64 sequences the tcgen05 kernel takes its units longest first;
+ * when total_tokens_hint is below B x (max_seq_len + T) (lengths differ), the
  * chunk is the cluster slots' even share of all tiles. The hint only sizes the
  * plan: any lengths give correct results.
  * Returns MLA_OK or MLA_ERR_INVALID_ARGUMENT / MLA_ERR_UNSUPPORTED.

@@ -81,6 +81,20 @@ def test_plan_ragged_hint_uses_more_splits(lib):
     assert m.plan(d1, 152).chunk_tokens <= m.plan(d0, 152).chunk_tokens
 
 
+@pytest.mark.parametrize("total", [20000, 300000, 1000000])
+def test_plan_ragged_full_chunks_fit_one_wave(lib, total):
+    """A ragged batch (2..64 sequences, lengths summed in the hint): however the lengths fall, its
+    full chunks number at most total / chunk, and the chunk is the clusters' even share of all
+    tiles, so they never outnumber the 76 cluster slots of a 152-SM part."""
+    d = desc(num_seqs=32, num_nodes=8, num_heads=16, max_seq_len=32767, slot_table_stride=32775, flags=0,
+             total_tokens_hint=total)
+    p = m.plan(d, 152)
+    tiles = -(-total // 64)
+    assert p.chunk_tokens == max(1, -(-tiles // 76)) * 64
+    assert total // p.chunk_tokens <= 76
+    assert p.num_splits * p.chunk_tokens >= 32767 + 8
+
+
 @pytest.mark.parametrize("bad", [dict(num_nodes=0), dict(num_nodes=65), dict(num_heads=0), dict(num_seqs=0),
                                  dict(slot_table_stride=100), dict(num_slots=0), dict(max_seq_len=-1),
                                  dict(softmax_scale=float("nan")), dict(out_dtype=7), dict(flags=1 << 9),

@@ -252,27 +252,55 @@ __device__ __forceinline__ void mma_smem_a(uint32_t d_tmem, uint64_t a_desc, uin
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// Largest of a tile's kKeys scores, as eight interleaved chains (max is exact in any order).
+// Three-input maximum (one instruction on this architecture; max is exact in any order).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Largest of a tile's kKeys scores, as eight interleaved chains of three-input maxima.
 __device__ __forceinline__ float max_of_keys(const float* x) {
+  static_assert(kKeys == 64, "chains of 8 + 3 x 16 + 8");
   float m[8];
 #pragma unroll
-  for (int u = 0; u < 8; ++u) m[u] = x[u];
-#pragma unroll
-  for (int k = 8; k < kKeys; k += 8)
-#pragma unroll
-    for (int u = 0; u < 8; ++u) m[u] = fmaxf(m[u], x[k + u]);
-  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+  for (int u = 0; u < 8; ++u) {
+    m[u] = max3(x[u], x[8 + u], x[16 + u]);
+    m[u] = max3(m[u], x[24 + u], x[32 + u]);
+    m[u] = max3(m[u], x[40 + u], x[48 + u]);
+    m[u] = fmaxf(m[u], x[56 + u]);
+  }
+  return max3(max3(m[0], m[1], m[2]), max3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
 }
 // Largest of the negated scores (the negated smallest score).
 __device__ __forceinline__ float max_of_neg_keys(const float* x) {
   float m[8];
 #pragma unroll
-  for (int u = 0; u < 8; ++u) m[u] = -x[u];
-#pragma unroll
-  for (int k = 8; k < kKeys; k += 8)
-#pragma unroll
-    for (int u = 0; u < 8; ++u) m[u] = fmaxf(m[u], -x[k + u]);
-  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+  for (int u = 0; u < 8; ++u) {
+    m[u] = max3(-x[u], -x[8 + u], -x[16 + u]);
+    m[u] = max3(m[u], -x[24 + u], -x[32 + u]);
+    m[u] = max3(m[u], -x[40 + u], -x[48 + u]);
+    m[u] = fmaxf(m[u], -x[56 + u]);
+  }
+  return max3(max3(m[0], m[1], m[2]), max3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+}
+// Two fp32 lanes per instruction (the packed f32x2 forms); each lane rounds exactly as fmaf / +.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n.reg .b64 ra, rb, rc, rd;\n"
+      "mov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %5};\nmov.b64 rc, {%6, %7};\n"
+      "fma.rn.f32x2 rd, ra, rb, rc;\nmov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n.reg .b64 ra, rb, rd;\n"
+      "mov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %5};\n"
+      "add.rn.f32x2 rd, ra, rb;\nmov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint32_t* v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
@@ -866,8 +894,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int k = 0; k < kKeys; k += 2) {
         // 2^23 + n - p / s rounded once to fp32 lands on the integer 2^23 + code, whose low 16
         // mantissa bits are the code
-        const float c0 = fmaf(-sv[k], inv_step, base);
-        const float c1 = fmaf(-sv[k + 1], inv_step, base);
+        const float2 cc = fma2(make_float2(sv[k], sv[k + 1]), make_float2(-inv_step, -inv_step), make_float2(base, base));
+        const float c0 = cc.x, c1 = cc.y;
         hv[k / 2] = __byte_perm(__float_as_uint(c0), __float_as_uint(c1), 0x5410);
       }
       const float top = base * __uint_as_float(sbits);
@@ -950,8 +978,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const float c0 = __uint_as_float(__byte_perm(wv[u], 0x4B000000u, 0x7610));
             const float c1 = __uint_as_float(__byte_perm(wv[u], 0x4B000000u, 0x7632));
             const int k = 8 * j + 2 * u;
-            sc[k] += fmaf(-c0, step, top);
-            sc[k + 1] += fmaf(-c1, step, top);
+            const float2 v = fma2(make_float2(c0, c1), make_float2(-step, -step), make_float2(top, top));
+            const float2 t2 = add2(make_float2(sc[k], sc[k + 1]), v);
+            sc[k] = t2.x;
+            sc[k + 1] = t2.y;
           }
         }
       }
@@ -984,11 +1014,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float lsum0 = 0.f, lsum1 = 0.f;  // two partial sums: shorter dependency chains
 #pragma unroll
       for (int k = 0; k < kKeys; k += 2) {
-        const float e0 = ex2(fmaf(sc[k], a.scale_log2, neg_m));
-        const float e1 = ex2(fmaf(sc[k + 1], a.scale_log2, neg_m));
+        const float2 x = fma2(make_float2(sc[k], sc[k + 1]), make_float2(a.scale_log2, a.scale_log2),
+                              make_float2(neg_m, neg_m));
+        const float e0 = ex2(x.x);
+        const float e1 = ex2(x.y);
         pk[k / 2] = pack_bf16(e0, e1);
-        lsum0 += e0;
-        lsum1 += e1;
+        const float2 ls = add2(make_float2(lsum0, lsum1), make_float2(e0, e1));
+        lsum0 = ls.x;
+        lsum1 = ls.y;
       }
       l_run += lsum0 + lsum1;
 

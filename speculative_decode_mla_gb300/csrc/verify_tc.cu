@@ -63,7 +63,7 @@ constexpr int kBlockBytes = kKeys * 128;            // 64 rows x 128 B (one 64-d
 constexpr int kRopeBytes = kKeys * 64;              // 64 rows x 64 B: this CTA's 32 RoPE dims, 64B swizzle
 constexpr int kStageBytes = 4 * kBlockBytes + kRopeBytes;  // 4 value blocks + the RoPE half
 constexpr int kXCodeBytes = kRows * kKeys * 2;      // 16-bit codes of the partial scores of one tile
-constexpr int kXBytes = kXCodeBytes + kRows * 8;    // + each row's reference and scale
+constexpr int kXBytes = kXCodeBytes + kRows * 8;    // + each row's grid (top, step)
 constexpr int kSmemP = kStages * kStageBytes;       // P (bf16, 128 rows x 64 positions, 128B swizzle)
 constexpr int kSmemQR = kSmemP + kRows * 128;       // the CTA's 32 RoPE dims of Q (128 rows x 64 B, 64B swizzle)
 constexpr int kSmemX = kSmemQR + kRows * 64;        // two exchange buffers
@@ -164,8 +164,8 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
 // cluster_scope: the phase is completed from the partner CTA (st.async bytes, remote arrive), a
 // release at cluster scope; it is polled relaxed and, once seen, acquired by one fence restricted
 // to shared::cluster memory, which is cheaper than an acquiring poll.
-// A probe of an mbarrier costs ~200 cycles even when the phase has completed, and so does reading
-// the clock: the first probe goes out before the clock is read.
+// A probe of an mbarrier costs over a hundred cycles even when the phase has completed, and
+// reading the clock costs some too: the first probe goes out before the clock is read.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                          bool cluster_scope = false) {
   if (cluster_scope) {

@@ -140,6 +140,7 @@ SHAPES = [
     ([77, 300], 3, 5, "star"),      # rows per sequence not a multiple of 8 / 128
     ([2000], 16, 8, "chain"),       # chain tree: causal tail
     ([5000, 4500, 6000], 9, 13, "random"),  # several tiles and a ragged tail per sequence
+    ([3000, 700, 5000], 16, 16, "random"),  # several sequences of two row tiles each, longest first
     ([(i * 53) % 700 for i in range(64)], 3, 4, "random"),  # 64 sequences: the longest-first unit order
     ([(i * 97) % 900 for i in range(70)], 2, 2, "random"),  # 70 sequences: units in index order
 ]
